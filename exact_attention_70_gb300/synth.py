@@ -1,0 +1,164 @@
+"""Seeded synthetic inputs shared by the tests, the smoke check and the benchmark.
+
+This module holds no attention arithmetic: it only draws numbers.  Both the CUDA path and the
+oracle receive exactly the tensors built here (bf16 bits drawn on the host), so they see
+identical inputs.
+
+Recipes (the shapes of the pages' workloads; there is no dataset):
+  * Q, K, V entries are iid N(0, 1) drawn in fp32 and rounded to bf16;
+  * sequence lengths are drawn uniformly with ``torch.randint`` from a generator seeded with
+    ``1000 + config id``;
+  * the paged cache's physical pages are a ``torch.randperm`` of the pool, the pool holding
+    exactly sum_b ceil(L_b / page_size) pages;
+  * large tensors are drawn in fixed-size blocks, block ``i`` from its own generator seeded
+    with ``seed * 1_000_003 + stream * 65_537 + i``, so a tensor's bits do not depend on how
+    many threads drew it.
+"""
+from __future__ import annotations
+
+import math
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field
+
+import torch
+
+_BLOCK = 1 << 22
+
+
+def randn_bf16(shape, seed: int, stream: int = 0) -> torch.Tensor:
+    """iid N(0,1) rounded to bf16, on the host, reproducible for (shape, seed, stream)."""
+    numel = math.prod(shape)
+    out = torch.empty(numel, dtype=torch.bfloat16)
+    nblk = (numel + _BLOCK - 1) // _BLOCK
+
+    def fill(i):
+        s, e = i * _BLOCK, min(numel, (i + 1) * _BLOCK)
+        g = torch.Generator().manual_seed(seed * 1_000_003 + stream * 65_537 + i)
+        out[s:e].copy_(torch.randn(e - s, generator=g, dtype=torch.float32))
+
+    if nblk <= 2:
+        for i in range(nblk):
+            fill(i)
+    else:
+        with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, range(nblk)))
+    return out.view(*shape)
+
+
+@dataclass
+class PrefillCase:
+    """Packed varlen prefill inputs: q [total_q, Hq, d], k/v [total_k, Hkv, d]."""
+    name: str
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    cu_seqlens_q: torch.Tensor
+    cu_seqlens_k: torch.Tensor
+    max_seqlen_q: int
+    max_seqlen_k: int
+    softmax_scale: float
+    causal: bool
+    window_left: int = -1
+    window_right: int = -1
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def batch(self):
+        return len(self.cu_seqlens_q) - 1
+
+
+@dataclass
+class DecodeCase:
+    """Decode inputs: q [batch, Hq, d]; caches [num_pages, page_size, Hkv, d]."""
+    name: str
+    q: torch.Tensor
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    cache_seqlens: torch.Tensor
+    block_table: torch.Tensor
+    page_size: int
+    softmax_scale: float
+    num_splits: int = 0
+    meta: dict = field(default_factory=dict)
+
+
+def cu_from_lengths(lengths) -> torch.Tensor:
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + int(n))
+    return torch.tensor(cu, dtype=torch.int32)
+
+
+def prefill_case(lengths_q, Hq, Hkv, d, causal, seed, lengths_k=None, window=(-1, -1),
+                 scale=None, name="prefill") -> PrefillCase:
+    lengths_k = list(lengths_q) if lengths_k is None else list(lengths_k)
+    cu_q, cu_k = cu_from_lengths(lengths_q), cu_from_lengths(lengths_k)
+    tq, tk = int(cu_q[-1]), int(cu_k[-1])
+    return PrefillCase(
+        name=name,
+        q=randn_bf16((tq, Hq, d), seed, 1),
+        k=randn_bf16((tk, Hkv, d), seed, 2),
+        v=randn_bf16((tk, Hkv, d), seed, 3),
+        cu_seqlens_q=cu_q, cu_seqlens_k=cu_k,
+        max_seqlen_q=max([0] + [int(x) for x in lengths_q]),
+        max_seqlen_k=max([0] + [int(x) for x in lengths_k]),
+        softmax_scale=d ** -0.5 if scale is None else scale, causal=bool(causal),
+        window_left=window[0], window_right=window[1],
+    )
+
+
+def decode_case(lengths, Hq, Hkv, d, page_size, seed, max_pages=None, num_splits=0,
+                scale=None, name="decode") -> DecodeCase:
+    g = torch.Generator().manual_seed(seed)
+    pages_per = [(int(n) + page_size - 1) // page_size for n in lengths]
+    num_pages = max(1, sum(pages_per))
+    max_pages = max([1] + pages_per) if max_pages is None else max_pages
+    perm = torch.randperm(num_pages, generator=g).to(torch.int32)
+    bt = torch.zeros((len(lengths), max_pages), dtype=torch.int32)
+    off = 0
+    for b, n in enumerate(pages_per):
+        bt[b, :n] = perm[off:off + n]
+        off += n
+    return DecodeCase(
+        name=name,
+        q=randn_bf16((len(lengths), Hq, d), seed, 1),
+        k_cache=randn_bf16((num_pages, page_size, Hkv, d), seed, 2),
+        v_cache=randn_bf16((num_pages, page_size, Hkv, d), seed, 3),
+        cache_seqlens=torch.tensor([int(n) for n in lengths], dtype=torch.int32),
+        block_table=bt, page_size=page_size,
+        softmax_scale=d ** -0.5 if scale is None else scale, num_splits=num_splits,
+    )
+
+
+# ---- the five workload configurations ------------------------------------------------
+
+CONFIG_NAMES = {
+    1: "single-head non-causal B=1 H=1 N=128 d=64",
+    2: "causal prefill B=4 Hq=Hkv=16 N=4096 d=128",
+    3: "varlen GQA causal prefill 8 seqs L~U[512,8192] Hq=32 Hkv=4 d=128",
+    4: "paged decode batch=64 L~U[1024,32768] page=256 Hq=32 Hkv=8 d=128",
+    5: "sliding-window causal prefill B=1 N=32768 Hq=32 Hkv=8 d=128 window=(4096,0)",
+}
+
+
+def config_case(cfg: int):
+    seed = 1000 + cfg
+    if cfg == 1:
+        c = prefill_case([128], 1, 1, 64, False, seed, name="cfg1")
+    elif cfg == 2:
+        c = prefill_case([4096] * 4, 16, 16, 128, True, seed, name="cfg2")
+    elif cfg == 3:
+        g = torch.Generator().manual_seed(seed)
+        lengths = torch.randint(512, 8192 + 1, (8,), generator=g).tolist()
+        c = prefill_case(lengths, 32, 4, 128, True, seed, name="cfg3")
+    elif cfg == 4:
+        g = torch.Generator().manual_seed(seed)
+        lengths = torch.randint(1024, 32768 + 1, (64,), generator=g).tolist()
+        c = decode_case(lengths, 32, 8, 128, 256, seed + 7, max_pages=128, name="cfg4")
+    elif cfg == 5:
+        c = prefill_case([32768], 32, 8, 128, True, seed, window=(4096, 0), name="cfg5")
+    else:
+        raise ValueError(cfg)
+    c.meta["config"] = CONFIG_NAMES[cfg]
+    return c

@@ -1,0 +1,369 @@
+/*
+ * attn_oracle.c -- the oracle for exact scaled-dot-product attention.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code, header, table or
+ * helper with the CUDA path and includes nothing from it.
+ *
+ * It is the plain definition, written out in fp64, and deliberately slow:
+ *
+ *   "Attention kernels: FlashAttention and PagedAttention" (arganzheng.life), section 二.1-二.2:
+ *     for one head, S = scale * Q K^T, P = softmax(S) row-wise, O = P V, with S and P
+ *     materialised.  Here every query row materialises its full row of S and of P
+ *     (Lk doubles each) before O is formed; nothing is tiled, fused or reordered.
+ *   same page, section 四.3: the per-row log-sum-exp L = m + log(sum exp(s - m)), natural log.
+ *   "04 · FA4 (CuTeDSL) and engineering interfaces" (llm-infra-atlas), sections 4-6:
+ *     varlen batches through cu_seqlens prefix sums (section 4), query head h reads kv head
+ *     h / (Hq/Hkv) (section 5), paged K/V through block_table (section 6.1), split-KV partials
+ *     merged by LSE (section 6.2), causal aligned bottom-right for the kv-cache call
+ *     (section 6.2) and the sliding window [i - w_left, i + w_right] (section 7 table).
+ *
+ * Readings where the pages are silent or disagree (each is also listed in the design notes):
+ *   - causal is aligned bottom-right everywhere: key j is visible to query i iff
+ *     j <= i + (Lk - Lq) (+ w_right when not causal); this equals top-left when Lq == Lk;
+ *   - window follows the API's (w_left, w_right) pair; -1 means unbounded on that side;
+ *     causal forces w_right = 0;
+ *   - a row with no visible key has O = 0 and LSE = -inf (no epsilon anywhere);
+ *   - an empty split has LSE = -inf and weight 0 in the merge.
+ *
+ * Inputs are either fp64 (dtype 0) or bf16 bit patterns (dtype 1); bf16 is widened to fp64
+ * exactly.  All arithmetic is fp64.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_F64 0
+#define ORACLE_BF16 1
+
+typedef struct {
+    long long flops;       /* 2d per visible (query, key) pair for QK^T + 2d for PV */
+    long long s_elems;     /* elements of S materialised (written once, read once by softmax) */
+    long long p_elems;     /* elements of P materialised (written once, read once by PV) */
+    long long qkvo_bytes;  /* bf16 bytes of Q, K, V read once and O written once */
+} oracle_counts_t;
+
+/* ---- element access ------------------------------------------------------------------ */
+
+static double bf16_to_f64(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Copy n consecutive elements starting at element index idx into dst as fp64. */
+static void load_row(const void* base, int dtype, int64_t idx, int n, double* dst) {
+    if (dtype == ORACLE_F64) {
+        const double* p = (const double*)base + idx;
+        for (int e = 0; e < n; ++e) dst[e] = p[e];
+    } else {
+        const uint16_t* p = (const uint16_t*)base + idx;
+        for (int e = 0; e < n; ++e) dst[e] = bf16_to_f64(p[e]);
+    }
+}
+
+/* ---- the visibility rule -------------------------------------------------------------- */
+
+/* Is key j visible to query row i of a sequence with Lq queries and Lk keys?
+ * Bottom-right alignment: query i sits at absolute key position i + (Lk - Lq). */
+int oracle_allowed(long long i, long long j, long long Lq, long long Lk, int causal,
+                   int window_left, int window_right) {
+    if (j < 0 || j >= Lk || i < 0 || i >= Lq) return 0;
+    long long pos = i + (Lk - Lq);
+    int wr = causal ? 0 : window_right;
+    if (wr >= 0 && j > pos + wr) return 0;
+    if (window_left >= 0 && j < pos - window_left) return 0;
+    return 1;
+}
+
+/* ---- one query row of standard attention ---------------------------------------------- */
+
+/*
+ * Materialise one row of S and P for query vector qrow over the keys whose element offsets
+ * are koff[0..Lk) (the same offsets index V), then form O and the row's LSE.
+ * vis[j] != 0 marks visible keys.  s_row and p_row are caller scratch of Lk doubles.
+ */
+static void attention_row(const double* qrow, const void* k, const void* v, int dtype,
+                          const int64_t* koff, const unsigned char* vis, int64_t Lk, int d,
+                          double scale, double* s_row, double* p_row, double* kbuf,
+                          double* out, double* lse, long long* pairs) {
+    /* S row: s_j = scale * <q, k_j> for visible keys, -inf otherwise. */
+    long long visible = 0;
+    for (int64_t j = 0; j < Lk; ++j) {
+        if (!vis[j]) { s_row[j] = -INFINITY; continue; }
+        load_row(k, dtype, koff[j], d, kbuf);
+        double acc = 0.0;
+        for (int e = 0; e < d; ++e) acc += qrow[e] * kbuf[e];
+        s_row[j] = scale * acc;
+        ++visible;
+    }
+    if (pairs) *pairs += visible;
+    for (int e = 0; e < d; ++e) out[e] = 0.0;
+    if (visible == 0) {          /* no visible key: O = 0, LSE = -inf */
+        for (int64_t j = 0; j < Lk; ++j) p_row[j] = 0.0;
+        *lse = -INFINITY;
+        return;
+    }
+    /* P row: exp(s - m) / sum exp(s - m). */
+    double m = -INFINITY;
+    for (int64_t j = 0; j < Lk; ++j) if (s_row[j] > m) m = s_row[j];
+    double denom = 0.0;
+    for (int64_t j = 0; j < Lk; ++j) {
+        p_row[j] = vis[j] ? exp(s_row[j] - m) : 0.0;
+        denom += p_row[j];
+    }
+    for (int64_t j = 0; j < Lk; ++j) p_row[j] /= denom;
+    /* O row: sum_j P_j v_j. */
+    for (int64_t j = 0; j < Lk; ++j) {
+        if (p_row[j] == 0.0) continue;
+        load_row(v, dtype, koff[j], d, kbuf);
+        for (int e = 0; e < d; ++e) out[e] += p_row[j] * kbuf[e];
+    }
+    *lse = m + log(denom);
+}
+
+/* Sequence index containing packed token t (cu has batch + 1 entries). */
+static int find_seq(const int32_t* cu, int batch, int64_t t) {
+    int lo = 0, hi = batch - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) / 2;
+        if (cu[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+static int check_common(int batch, int Hq, int Hkv, int d) {
+    if (batch < 0 || Hq <= 0 || Hkv <= 0 || d <= 0) return -1;
+    if (Hq % Hkv != 0) return -1;
+    return 0;
+}
+
+/* ---- prefill: every row, with the standard implementation's accounting ---------------- */
+
+/*
+ * q [total_q, Hq, d], k and v [total_k, Hkv, d]; out [total_q, Hq, d]; lse [Hq, total_q].
+ * Sequence b owns query rows [cu_q[b], cu_q[b+1]) and key rows [cu_k[b], cu_k[b+1]).
+ */
+int oracle_attn_fwd(const void* q, const void* k, const void* v, int dtype,
+                    const int32_t* cu_q, const int32_t* cu_k, int batch, int Hq, int Hkv,
+                    int d, double scale, int causal, int window_left, int window_right,
+                    double* out, double* lse, long long total_q, oracle_counts_t* counts) {
+    if (check_common(batch, Hq, Hkv, d)) return -1;
+    for (int b = 0; b < batch; ++b)
+        if (cu_q[b + 1] < cu_q[b] || cu_k[b + 1] < cu_k[b]) return -1;
+    if (batch > 0 && cu_q[batch] > total_q) return -1;
+    const int g = Hq / Hkv;
+    long long flops = 0, s_el = 0, p_el = 0, qkvo = 0;
+    const long long n_bh = (long long)batch * Hq;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : flops, s_el, p_el, qkvo)
+    for (long long bh = 0; bh < n_bh; ++bh) {
+        const int b = (int)(bh / Hq), h = (int)(bh % Hq), kvh = h / g;
+        const int64_t Lq = cu_q[b + 1] - cu_q[b], Lk = cu_k[b + 1] - cu_k[b];
+        int64_t* koff = (int64_t*)malloc(sizeof(int64_t) * (Lk > 0 ? Lk : 1));
+        unsigned char* vis = (unsigned char*)malloc(Lk > 0 ? Lk : 1);
+        double* s_row = (double*)malloc(sizeof(double) * (Lk > 0 ? Lk : 1));
+        double* p_row = (double*)malloc(sizeof(double) * (Lk > 0 ? Lk : 1));
+        double* qrow = (double*)malloc(sizeof(double) * d);
+        double* kbuf = (double*)malloc(sizeof(double) * d);
+        for (int64_t j = 0; j < Lk; ++j) koff[j] = ((int64_t)(cu_k[b] + j) * Hkv + kvh) * d;
+        for (int64_t i = 0; i < Lq; ++i) {
+            const int64_t t = cu_q[b] + i;
+            for (int64_t j = 0; j < Lk; ++j)
+                vis[j] = (unsigned char)oracle_allowed(i, j, Lq, Lk, causal, window_left,
+                                                       window_right);
+            load_row(q, dtype, (t * Hq + h) * d, d, qrow);
+            long long pairs = 0;
+            attention_row(qrow, k, v, dtype, koff, vis, Lk, d, scale, s_row, p_row, kbuf,
+                          out + (t * Hq + h) * d, lse + (int64_t)h * total_q + t, &pairs);
+            flops += 4LL * d * pairs;
+            s_el += Lk;
+            p_el += Lk;
+        }
+        qkvo += 2LL * d * (2 * Lq + 2 * Lk); /* Q and O rows, K and V rows, bf16 */
+        free(koff); free(vis); free(s_row); free(p_row); free(qrow); free(kbuf);
+    }
+    if (counts) {
+        counts->flops = flops;
+        counts->s_elems = s_el;
+        counts->p_elems = p_el;
+        counts->qkvo_bytes = qkvo;
+    }
+    return 0;
+}
+
+/* ---- prefill: a chosen set of (packed token, query head) rows ------------------------- */
+
+int oracle_attn_fwd_rows(const void* q, const void* k, const void* v, int dtype,
+                         const int32_t* cu_q, const int32_t* cu_k, int batch, int Hq, int Hkv,
+                         int d, double scale, int causal, int window_left, int window_right,
+                         const int64_t* row_tok, const int32_t* row_head, long long nrows,
+                         double* out, double* lse) {
+    if (check_common(batch, Hq, Hkv, d) || batch == 0) return -1;
+    const int g = Hq / Hkv;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 4) reduction(| : bad)
+    for (long long r = 0; r < nrows; ++r) {
+        const int64_t t = row_tok[r];
+        const int h = row_head[r];
+        if (t < cu_q[0] || t >= cu_q[batch] || h < 0 || h >= Hq) { bad |= 1; continue; }
+        const int b = find_seq(cu_q, batch, t), kvh = h / g;
+        const int64_t Lq = cu_q[b + 1] - cu_q[b], Lk = cu_k[b + 1] - cu_k[b];
+        const int64_t i = t - cu_q[b];
+        int64_t* koff = (int64_t*)malloc(sizeof(int64_t) * (Lk > 0 ? Lk : 1));
+        unsigned char* vis = (unsigned char*)malloc(Lk > 0 ? Lk : 1);
+        double* s_row = (double*)malloc(sizeof(double) * (Lk > 0 ? Lk : 1));
+        double* p_row = (double*)malloc(sizeof(double) * (Lk > 0 ? Lk : 1));
+        double* qrow = (double*)malloc(sizeof(double) * d);
+        double* kbuf = (double*)malloc(sizeof(double) * d);
+        for (int64_t j = 0; j < Lk; ++j) {
+            koff[j] = ((int64_t)(cu_k[b] + j) * Hkv + kvh) * d;
+            vis[j] = (unsigned char)oracle_allowed(i, j, Lq, Lk, causal, window_left,
+                                                   window_right);
+        }
+        load_row(q, dtype, (t * Hq + h) * d, d, qrow);
+        attention_row(qrow, k, v, dtype, koff, vis, Lk, d, scale, s_row, p_row, kbuf,
+                      out + r * d, lse + r, NULL);
+        free(koff); free(vis); free(s_row); free(p_row); free(qrow); free(kbuf);
+    }
+    return bad ? -1 : 0;
+}
+
+/* ---- merge of split partials ------------------------------------------------------------ */
+
+/*
+ * "Attention kernels: FlashAttention and PagedAttention", section 六.3: partials
+ * (m_i, l_i, O_i) with O_i already normalised by l_i merge as
+ *   m = max_i m_i,  l = sum_i l_i e^(m_i - m),  O = sum_i O_i l_i e^(m_i - m) / l.
+ * A split with l_i == 0 (no visible key) contributes nothing.  Result LSE = m + log l.
+ */
+int oracle_merge(int nsplits, int d, const double* m_i, const double* l_i, const double* o_i,
+                 double* out, double* lse) {
+    double m = -INFINITY;
+    for (int s = 0; s < nsplits; ++s)
+        if (l_i[s] > 0.0 && m_i[s] > m) m = m_i[s];
+    for (int e = 0; e < d; ++e) out[e] = 0.0;
+    if (m == -INFINITY) { *lse = -INFINITY; return 0; }
+    double l = 0.0;
+    for (int s = 0; s < nsplits; ++s)
+        if (l_i[s] > 0.0) l += l_i[s] * exp(m_i[s] - m);
+    for (int s = 0; s < nsplits; ++s) {
+        if (!(l_i[s] > 0.0)) continue;
+        const double w = l_i[s] * exp(m_i[s] - m) / l;
+        for (int e = 0; e < d; ++e) out[e] += w * o_i[(int64_t)s * d + e];
+    }
+    *lse = m + log(l);
+    return 0;
+}
+
+/* ---- decode over a paged KV cache ------------------------------------------------------- */
+
+/*
+ * q [batch, Hq, d] (one query per sequence); k_cache and v_cache
+ * [num_pages, page_size, Hkv, d]; key j of sequence b lives in physical page
+ * block_table[b * max_pages + j / page_size] at offset j % page_size
+ * ("Attention kernels ...", section 六.1; "04 · FA4 ...", section 6.1).
+ * All cache_seqlens[b] keys are visible (bottom-right causal with Lq = 1).
+ *
+ * num_splits == 0: one pass over all keys.  num_splits >= 1: split s takes keys
+ * [s*C, min((s+1)*C, L)) with C = ceil(L / num_splits); each split materialises its own S and P
+ * rows and yields (m_s, l_s, O_s); the splits are merged by oracle_merge.
+ *
+ * Rows are (b, h) pairs; rows_b == NULL means all batch*Hq rows in (b, h) order.
+ * out [nrows, d], lse [nrows].  Returns -1 on an invalid page index or length.
+ */
+int oracle_decode(const void* q, const void* k_cache, const void* v_cache, int dtype,
+                  const int32_t* cache_seqlens, const int32_t* block_table, int max_pages,
+                  int page_size, int num_pages, int batch, int Hq, int Hkv, int d,
+                  double scale, int num_splits, const int32_t* rows_b, const int32_t* rows_h,
+                  long long nrows, double* out, double* lse) {
+    if (check_common(batch, Hq, Hkv, d) || page_size <= 0 || num_splits < 0) return -1;
+    const int g = Hq / Hkv;
+    const long long n = rows_b ? nrows : (long long)batch * Hq;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (long long r = 0; r < n; ++r) {
+        const int b = rows_b ? rows_b[r] : (int)(r / Hq);
+        const int h = rows_b ? rows_h[r] : (int)(r % Hq);
+        if (b < 0 || b >= batch || h < 0 || h >= Hq) { bad |= 1; continue; }
+        const int kvh = h / g;
+        const int64_t L = cache_seqlens[b];
+        if (L < 0 || L > (int64_t)max_pages * page_size) { bad |= 1; continue; }
+        int64_t* koff = (int64_t*)malloc(sizeof(int64_t) * (L > 0 ? L : 1));
+        int page_bad = 0;
+        for (int64_t j = 0; j < L; ++j) {
+            const int32_t page = block_table[(int64_t)b * max_pages + j / page_size];
+            if (page < 0 || page >= num_pages) { page_bad = 1; koff[j] = 0; continue; }
+            koff[j] = (((int64_t)page * page_size + j % page_size) * Hkv + kvh) * d;
+        }
+        if (page_bad) { bad |= 1; free(koff); continue; }
+        double* qrow = (double*)malloc(sizeof(double) * d);
+        double* kbuf = (double*)malloc(sizeof(double) * d);
+        double* s_row = (double*)malloc(sizeof(double) * (L > 0 ? L : 1));
+        double* p_row = (double*)malloc(sizeof(double) * (L > 0 ? L : 1));
+        unsigned char* vis = (unsigned char*)malloc(L > 0 ? L : 1);
+        load_row(q, dtype, ((int64_t)b * Hq + h) * d, d, qrow);
+        if (num_splits == 0) {
+            for (int64_t j = 0; j < L; ++j)
+                vis[j] = (unsigned char)oracle_allowed(0, j, 1, L, 1, -1, -1);
+            attention_row(qrow, k_cache, v_cache, dtype, koff, vis, L, d, scale, s_row, p_row,
+                          kbuf, out + r * d, lse + r, NULL);
+        } else {
+            const int S = num_splits;
+            const int64_t C = (L + S - 1) / S;
+            double* m_i = (double*)malloc(sizeof(double) * S);
+            double* l_i = (double*)malloc(sizeof(double) * S);
+            double* o_i = (double*)malloc(sizeof(double) * S * d);
+            for (int s = 0; s < S; ++s) {
+                const int64_t j0 = (int64_t)s * C < L ? (int64_t)s * C : L;
+                const int64_t j1 = j0 + C < L ? j0 + C : L;
+                const int64_t n_s = j1 - j0;
+                for (int64_t j = 0; j < n_s; ++j)
+                    vis[j] = (unsigned char)oracle_allowed(0, j0 + j, 1, L, 1, -1, -1);
+                double lse_s;
+                attention_row(qrow, k_cache, v_cache, dtype, koff + j0, vis, n_s, d, scale,
+                              s_row, p_row, kbuf, o_i + (int64_t)s * d, &lse_s, NULL);
+                /* express the partial as (m_s, l_s) with O_s normalised */
+                if (lse_s == -INFINITY) { m_i[s] = -INFINITY; l_i[s] = 0.0; }
+                else {
+                    double m = -INFINITY;
+                    for (int64_t j = 0; j < n_s; ++j) if (s_row[j] > m) m = s_row[j];
+                    double l = 0.0;
+                    for (int64_t j = 0; j < n_s; ++j)
+                        if (vis[j]) l += exp(s_row[j] - m);
+                    m_i[s] = m;
+                    l_i[s] = l;
+                }
+            }
+            oracle_merge(S, d, m_i, l_i, o_i, out + r * d, lse + r);
+            free(m_i); free(l_i); free(o_i);
+        }
+        free(koff); free(qrow); free(kbuf); free(s_row); free(p_row); free(vis);
+    }
+    return bad ? -1 : 0;
+}
+
+/* ---- the tiled method's traffic model (for the roofline discussion) -------------------- */
+
+/*
+ * "Attention kernels ...", section 三.3: with Q read once and O written once, and K and V
+ * each read once per query block of Br rows, the HBM bytes of one head are
+ * 2*N*d*2 (Q, O) + 2 * (N / Br) * N*d*2 (K, V re-reads), bf16.
+ */
+long long oracle_tiled_traffic_bytes(long long N, long long d, long long Br) {
+    const long long blocks = (N + Br - 1) / Br;
+    return 2 * N * d * 2 + 2 * blocks * N * d * 2;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,230 @@
+"""Python face of the fp64 attention oracle (``attn_oracle.c``).
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` may import this module.  It never imports the
+CUDA package, and the CUDA package never imports it.
+
+Every function takes host arrays (numpy, or CPU torch tensors which are viewed without a
+copy of their bits) and returns fp64 numpy arrays.  bf16 inputs are passed as their raw
+16-bit patterns and widened to fp64 exactly inside the C code.
+
+Sources (page titles and sections):
+  * "Attention kernels: FlashAttention and PagedAttention" (arganzheng.life),
+    section 二 (standard attention, its byte and FLOP accounting), 四.3 (LSE),
+    六.1 (block-table addressing), 六.3 (merge of split partials), 七 (varlen, causal,
+    sliding window);
+  * "04 · FA4 (CuTeDSL) and engineering interfaces" (llm-infra-atlas), sections 4-7
+    (cu_seqlens, pack_gqa head mapping, paged KV, split-KV, bottom-right causal, window).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F64, BF16 = 0, 1
+
+
+class Counts(ctypes.Structure):
+    _fields_ = [("flops", ctypes.c_longlong), ("s_elems", ctypes.c_longlong),
+                ("p_elems", ctypes.c_longlong), ("qkvo_bytes", ctypes.c_longlong)]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (fp64, OpenMP, no fast-math)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i32, i64, dbl, ll = ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_longlong
+            lib.oracle_allowed.restype = i32
+            lib.oracle_allowed.argtypes = [ll, ll, ll, ll, i32, i32, i32]
+            lib.oracle_attn_fwd.restype = i32
+            lib.oracle_attn_fwd.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, dbl, i32,
+                                            i32, i32, P, P, ll, P]
+            lib.oracle_attn_fwd_rows.restype = i32
+            lib.oracle_attn_fwd_rows.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, dbl,
+                                                 i32, i32, i32, P, P, ll, P, P]
+            lib.oracle_merge.restype = i32
+            lib.oracle_merge.argtypes = [i32, i32, P, P, P, P, P]
+            lib.oracle_decode.restype = i32
+            lib.oracle_decode.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                          dbl, i32, P, P, ll, P, P]
+            lib.oracle_tiled_traffic_bytes.restype = ll
+            lib.oracle_tiled_traffic_bytes.argtypes = [ll, ll, ll]
+            lib.oracle_num_threads.restype = i32
+            lib.oracle_num_threads.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def _host(x, dtype_hint=None):
+    """Return (contiguous numpy array, oracle dtype code) for an input tensor."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach()
+            if x.device.type != "cpu":
+                raise ValueError("the oracle takes host tensors only")
+            x = x.contiguous()
+            if x.dtype == torch.bfloat16:
+                return x.view(torch.int16).numpy().view(np.uint16), BF16
+            if x.dtype == torch.float64:
+                return x.numpy(), F64
+            if x.dtype == torch.int32:
+                return x.numpy(), None
+            if x.dtype == torch.int64:
+                return x.numpy(), None
+            raise ValueError(f"unsupported dtype {x.dtype}")
+    except ImportError:  # pragma: no cover
+        pass
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float64:
+        return x, F64
+    if x.dtype == np.uint16:
+        return x, BF16
+    return x, None
+
+
+def _i32(x):
+    a, _ = _host(x)
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def allowed(i, j, Lq, Lk, causal, window_left=-1, window_right=-1) -> bool:
+    """The visibility rule (bottom-right aligned causal / sliding window)."""
+    return bool(_load().oracle_allowed(i, j, Lq, Lk, int(causal), window_left, window_right))
+
+
+def attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, softmax_scale, causal=False,
+             window_left=-1, window_right=-1, with_counts=False):
+    """Standard attention over every row.  q [total_q, Hq, d]; k, v [total_k, Hkv, d].
+
+    Returns (out [total_q, Hq, d] f64, lse [Hq, total_q] f64[, Counts]).
+    """
+    qa, dt = _host(q)
+    ka, dk = _host(k)
+    va, dv = _host(v)
+    if not (dt == dk == dv) or dt is None:
+        raise ValueError("q, k, v must share one dtype (bf16 or fp64)")
+    total_q, Hq, d = qa.shape
+    Hkv = ka.shape[1]
+    cu_q, cu_k = _i32(cu_seqlens_q), _i32(cu_seqlens_k)
+    batch = len(cu_q) - 1
+    out = np.zeros((total_q, Hq, d), np.float64)
+    lse = np.full((Hq, total_q), np.nan, np.float64)
+    counts = Counts()
+    rc = _load().oracle_attn_fwd(_ptr(qa), _ptr(ka), _ptr(va), dt, _ptr(cu_q), _ptr(cu_k), batch,
+                                 Hq, Hkv, d, float(softmax_scale), int(causal), window_left,
+                                 window_right, _ptr(out), _ptr(lse), total_q,
+                                 ctypes.byref(counts))
+    if rc != 0:
+        raise ValueError("oracle_attn_fwd rejected its arguments")
+    return (out, lse, counts) if with_counts else (out, lse)
+
+
+def attn_fwd_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, softmax_scale, row_tok, row_head,
+                  causal=False, window_left=-1, window_right=-1):
+    """Standard attention for chosen (packed token, query head) rows.
+
+    Returns (out [n, d] f64, lse [n] f64).
+    """
+    qa, dt = _host(q)
+    ka, _ = _host(k)
+    va, _ = _host(v)
+    total_q, Hq, d = qa.shape
+    Hkv = ka.shape[1]
+    cu_q, cu_k = _i32(cu_seqlens_q), _i32(cu_seqlens_k)
+    tok = np.ascontiguousarray(np.asarray(row_tok), dtype=np.int64)
+    head = np.ascontiguousarray(np.asarray(row_head), dtype=np.int32)
+    n = len(tok)
+    out = np.zeros((n, d), np.float64)
+    lse = np.zeros((n,), np.float64)
+    rc = _load().oracle_attn_fwd_rows(_ptr(qa), _ptr(ka), _ptr(va), dt, _ptr(cu_q), _ptr(cu_k),
+                                      len(cu_q) - 1, Hq, Hkv, d, float(softmax_scale),
+                                      int(causal), window_left, window_right, _ptr(tok),
+                                      _ptr(head), n, _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle_attn_fwd_rows rejected its arguments")
+    return out, lse
+
+
+def merge(m_i, l_i, o_i):
+    """Merge split partials (m_i, l_i, O_i normalised) -> (O, LSE)."""
+    m = np.ascontiguousarray(m_i, np.float64)
+    l = np.ascontiguousarray(l_i, np.float64)
+    o = np.ascontiguousarray(o_i, np.float64)
+    S, d = o.shape
+    out = np.zeros((d,), np.float64)
+    lse = np.zeros((1,), np.float64)
+    _load().oracle_merge(S, d, _ptr(m), _ptr(l), _ptr(o), _ptr(out), _ptr(lse))
+    return out, float(lse[0])
+
+
+def decode(q, k_cache, v_cache, cache_seqlens, block_table, softmax_scale, num_splits=0,
+           rows_b=None, rows_h=None):
+    """Decode (one query per sequence) over a paged cache.
+
+    q [batch, Hq, d]; k_cache, v_cache [num_pages, page_size, Hkv, d];
+    block_table [batch, max_pages] int32; cache_seqlens [batch] int32.
+    Returns (out [n, d], lse [n]) for the chosen (b, h) rows, or ([batch, Hq, d], [batch, Hq]).
+    """
+    qa, dt = _host(q)
+    ka, _ = _host(k_cache)
+    va, _ = _host(v_cache)
+    batch, Hq, d = qa.shape
+    num_pages, page_size, Hkv, _ = ka.shape
+    sl = _i32(cache_seqlens)
+    bt = _i32(block_table)
+    max_pages = bt.shape[1] if bt.ndim == 2 else 0
+    if rows_b is None:
+        n = batch * Hq
+        rb = rh = None
+    else:
+        rb = np.ascontiguousarray(np.asarray(rows_b), dtype=np.int32)
+        rh = np.ascontiguousarray(np.asarray(rows_h), dtype=np.int32)
+        n = len(rb)
+    out = np.zeros((n, d), np.float64)
+    lse = np.zeros((n,), np.float64)
+    rc = _load().oracle_decode(_ptr(qa), _ptr(ka), _ptr(va), dt, _ptr(sl), _ptr(bt), max_pages,
+                               page_size, num_pages, batch, Hq, Hkv, d, float(softmax_scale),
+                               int(num_splits), _ptr(rb) if rb is not None else None,
+                               _ptr(rh) if rh is not None else None, n, _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle_decode rejected its arguments (bad page index or length)")
+    if rows_b is None:
+        return out.reshape(batch, Hq, d), lse.reshape(batch, Hq)
+    return out, lse
+
+
+def tiled_traffic_bytes(N, d, Br) -> int:
+    return int(_load().oracle_tiled_traffic_bytes(N, d, Br))
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
