@@ -1,0 +1,207 @@
+"""ctypes binding of libattn.so: argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module checks tensor
+dtypes and shapes, allocates outputs and workspace with torch when the caller does not pass
+them, and forwards raw device pointers and the current CUDA stream.  If the library has not
+been built the first call raises ``AttnError`` -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported configuration",
+          -3: "workspace missing or too small", -4: "CUDA call failed",
+          -5: "a kernel wait exceeded its time limit", -6: "a device-side index was out of range"}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code, where):
+        super().__init__(f"{where}: {STATUS.get(code, code)} ({code})")
+        self.code = code
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libattn.so (built by ``__graft_entry__.build()`` / ``exact_attention_70_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                raise AttnError(-4, f"libattn.so not built (expected at {path})")
+            lib = ctypes.CDLL(path)
+            P, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            lib.attn_fwd.restype = i32
+            lib.attn_fwd.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
+                                     f32, i32, i32, i32, P, sz, P]
+            lib.attn_fwd_workspace_bytes.restype = sz
+            lib.attn_fwd_workspace_bytes.argtypes = [i32, i32, i32, i32]
+            lib.attn_decode_kvcache.restype = i32
+            lib.attn_decode_kvcache.argtypes = [P, P, P, P, P, i32, i32, P, P, i32, i32, i32, i32,
+                                                i32, i32, f32, P, sz, P]
+            lib.attn_decode_workspace_bytes.restype = sz
+            lib.attn_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
+            lib.attn_decode_num_splits.restype = i32
+            lib.attn_decode_num_splits.argtypes = [i32, i32, i32, i32, i32, i32]
+            lib.attn_get_device_status.restype = i32
+            lib.attn_get_device_status.argtypes = [P]
+            lib.attn_status_string.restype = ctypes.c_char_p
+            lib.attn_status_string.argtypes = [i32]
+            lib.attn_kv_block_range.restype = i32
+            lib.attn_kv_block_range.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32,
+                                                ctypes.POINTER(i32), ctypes.POINTER(i32)]
+            lib.attn_kv_block_masked.restype = i32
+            lib.attn_kv_block_masked.argtypes = [i32] * 9
+            _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t, name, dtype, ndim):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def attn_fwd_workspace_bytes(batch, max_seqlen_q, nheads_q, nheads_kv) -> int:
+    return int(load().attn_fwd_workspace_bytes(batch, max_seqlen_q, nheads_q, nheads_kv))
+
+
+def attn_decode_workspace_bytes(batch, nheads_q, head_dim, num_splits) -> int:
+    return int(load().attn_decode_workspace_bytes(batch, nheads_q, head_dim, num_splits))
+
+
+def attn_decode_num_splits(batch, nheads_q, nheads_kv, max_pages_per_seq, page_size, num_sms):
+    return int(load().attn_decode_num_splits(batch, nheads_q, nheads_kv, max_pages_per_seq,
+                                             page_size, num_sms))
+
+
+def attn_kv_block_range(i_min, i_max, seqlen_q, seqlen_k, block_n, causal, wl, wr):
+    lo, hi = ctypes.c_int(), ctypes.c_int()
+    rc = load().attn_kv_block_range(i_min, i_max, seqlen_q, seqlen_k, block_n, int(causal), wl,
+                                    wr, ctypes.byref(lo), ctypes.byref(hi))
+    if rc != 0:
+        raise AttnError(-1, "attn_kv_block_range")
+    return lo.value, hi.value
+
+
+def attn_kv_block_masked(j, i_min, i_max, seqlen_q, seqlen_k, block_n, causal, wl, wr) -> bool:
+    return bool(load().attn_kv_block_masked(j, i_min, i_max, seqlen_q, seqlen_k, block_n,
+                                            int(causal), wl, wr))
+
+
+def attn_get_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status code."""
+    return int(load().attn_get_device_status(_stream(stream)))
+
+
+def _workspace(nbytes, device, workspace):
+    if nbytes == 0:
+        return None
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise AttnError(-3, "workspace")
+        return workspace
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+             softmax_scale=None, causal=False, window_left=-1, window_right=-1,
+             out=None, lse=None, workspace=None, stream=None):
+    """Varlen prefill.  q [total_q, Hq, d], k/v [total_k, Hkv, d] bf16; cu_seqlens int32.
+
+    Returns (out [total_q, Hq, d] bf16, lse [Hq, total_q] fp32).
+    """
+    lib = load()
+    _check(q, "q", torch.bfloat16, 3)
+    _check(k, "k", torch.bfloat16, 3)
+    _check(v, "v", torch.bfloat16, 3)
+    _check(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _check(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    total_q, Hq, d = q.shape
+    total_k, Hkv, dk = k.shape
+    if v.shape != k.shape or dk != d:
+        raise ValueError("k and v must both be [total_k, Hkv, d] with q's d")
+    batch = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != batch + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
+    scale = d ** -0.5 if softmax_scale is None else float(softmax_scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    _check(out, "out", torch.bfloat16, 3)
+    _check(lse, "lse", torch.float32, 2)
+    nbytes = int(lib.attn_fwd_workspace_bytes(max(batch, 0), int(max_seqlen_q), Hq, Hkv))
+    ws = _workspace(nbytes, q.device, workspace)
+    rc = lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q),
+                      _ptr(cu_seqlens_k), batch, total_q, total_k, int(max_seqlen_q),
+                      int(max_seqlen_k), Hq, Hkv, d, scale, int(bool(causal)), int(window_left),
+                      int(window_right), _ptr(ws), nbytes, _stream(stream))
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd")
+    return out, lse
+
+
+def attn_decode_kvcache(q, k_cache, v_cache, cache_seqlens, block_table, softmax_scale=None,
+                        num_splits=0, out=None, lse=None, workspace=None, stream=None):
+    """Decode over a paged cache.  q [batch, Hq, d]; caches [num_pages, page_size, Hkv, d].
+
+    Returns (out [batch, Hq, d] bf16, lse [batch, Hq] fp32).
+    """
+    lib = load()
+    _check(q, "q", torch.bfloat16, 3)
+    _check(k_cache, "k_cache", torch.bfloat16, 4)
+    _check(v_cache, "v_cache", torch.bfloat16, 4)
+    _check(cache_seqlens, "cache_seqlens", torch.int32, 1)
+    _check(block_table, "block_table", torch.int32, 2)
+    batch, Hq, d = q.shape
+    num_pages, page_size, Hkv, dk = k_cache.shape
+    if v_cache.shape != k_cache.shape or dk != d:
+        raise ValueError("k_cache and v_cache must both be [num_pages, page_size, Hkv, d]")
+    if cache_seqlens.numel() != batch or block_table.shape[0] != batch:
+        raise ValueError("cache_seqlens and block_table must have one row per sequence")
+    scale = d ** -0.5 if softmax_scale is None else float(softmax_scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((batch, Hq), dtype=torch.float32, device=q.device)
+    _check(out, "out", torch.bfloat16, 3)
+    _check(lse, "lse", torch.float32, 2)
+    nbytes = int(lib.attn_decode_workspace_bytes(batch, Hq, d, int(num_splits)))
+    ws = _workspace(nbytes, q.device, workspace)
+    rc = lib.attn_decode_kvcache(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_seqlens),
+                                 _ptr(block_table), page_size, int(num_splits), _ptr(out),
+                                 _ptr(lse), batch, Hq, Hkv, d, block_table.shape[1], num_pages,
+                                 scale, _ptr(ws), nbytes, _stream(stream))
+    if rc != 0:
+        raise AttnError(rc, "attn_decode_kvcache")
+    return out, lse

@@ -1,0 +1,102 @@
+// kernels.h -- parameter blocks and launchers shared by the host API (attn_api.cu) and the
+// kernel translation units.  Nothing here is part of the public C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn {
+
+// Bits of the per-device status word the kernels raise instead of trapping.
+constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusBounds = 2u;
+
+// ---- prefill ----------------------------------------------------------------------------
+
+constexpr int kFwdBlockN = 128;     // keys per KV tile
+constexpr int kFwdTilesPerItem = 2; // Q tiles (of 128 packed rows) per work item
+constexpr int kFwdThreads = 320;    // 2 softmax warpgroups + TMA warp + MMA warp
+constexpr int kPrepThreads = 1024;
+constexpr int kPrepBins = 1024;     // cost histogram bins of the work-list sort
+
+// Workspace layout of attn_fwd: [header 256 B][prefix int32 (batch+1), 16-B aligned][items]
+struct FwdWorkspaceHeader {
+    int n_items;
+    int n_pairs;
+    int pad[62];
+};
+
+struct FwdPrepParams {
+    const int* cu_q;
+    const int* cu_k;
+    int* prefix;     // [batch + 1] work items per sequence, exclusive scan
+    int4* items;     // [capacity_pairs * Hkv]
+    FwdWorkspaceHeader* header;
+    unsigned* status;
+    int batch, total_q, total_k, max_seqlen_q, max_seqlen_k;
+    int Hkv, tpt, capacity_pairs;
+    int causal, wl, wr;
+};
+
+struct FwdParams {
+    CUtensorMap tm_q;  // 3-D over q   [total_q, Hq, d],  box {64, g, tpt}
+    CUtensorMap tm_k;  // 3-D over k   [total_k, Hkv, d], box {64, 1, 128}
+    CUtensorMap tm_v;  // 3-D over v   [total_k, Hkv, d], box {64, 1, 128}
+    __nv_bfloat16* out;
+    float* lse;
+    const int* cu_q;
+    const int* cu_k;
+    const int4* items;
+    const FwdWorkspaceHeader* header;
+    unsigned* status;
+    int Hq, Hkv, g, tpt, total_q;
+    int causal, wl, wr;
+    float scale_log2;  // softmax_scale * log2(e)
+};
+
+cudaError_t launch_fwd_prepare(const FwdPrepParams& p, cudaStream_t stream);
+cudaError_t launch_fwd(const FwdParams& p, int head_dim, int grid, cudaStream_t stream);
+int fwd_smem_bytes(int head_dim);
+
+// ---- decode -------------------------------------------------------------------------------
+
+constexpr int kDecChunk = 64;       // keys per pipeline stage
+constexpr int kDecThreads = 160;    // 4 MMA warps + 1 TMA warp
+constexpr int kDecRowsPerCta = 16;  // query heads of one kv group handled by one CTA
+
+struct DecParams {
+    CUtensorMap tm_k;  // 3-D over k_cache [num_pages*page_size, Hkv, d], box {64, 1, box_rows}
+    CUtensorMap tm_v;
+    const __nv_bfloat16* q;
+    __nv_bfloat16* out;
+    float* lse;
+    float* part_o;    // [batch, Hq, num_splits, d]  (num_splits > 1)
+    float* part_lse;  // [batch, Hq, num_splits]
+    const int* seqlens;
+    const int* block_table;
+    unsigned* status;
+    int batch, Hq, Hkv, g, hgroups;
+    int page_size, box_rows, max_pages, num_pages, num_splits;
+    float scale_log2;
+};
+
+struct CombineParams {
+    const float* part_o;
+    const float* part_lse;
+    __nv_bfloat16* out;
+    float* lse;
+    int rows;  // batch * Hq
+    int num_splits;
+};
+
+cudaError_t launch_decode(const DecParams& p, int head_dim, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, int head_dim, cudaStream_t stream);
+int decode_smem_bytes(int head_dim);
+
+// Configure the kernels' shared-memory limits on the current device (idempotent).
+cudaError_t configure_fwd_kernels();
+cudaError_t configure_decode_kernels();
+
+}  // namespace attn

@@ -1,0 +1,157 @@
+/*
+ * attn.h -- C ABI of libattn.so: exact tiled scaled-dot-product attention on GB300 (sm_103a).
+ *
+ * What is computed ("Attention kernels: FlashAttention and PagedAttention", section 二.1 and
+ * section 三.2; "04 · FA4 (CuTeDSL) and engineering interfaces", sections 3-7):
+ *   for every query row i of sequence b and query head h,
+ *     S_ij  = softmax_scale * <q_i,h , k_j,kvh>        kvh = h / (nheads_q / nheads_kv)
+ *     O_i,h = sum_j softmax_j(S_i.) v_j,kvh          over the keys j visible to row i
+ *     LSE   = log sum_j exp(S_ij)                    (natural log)
+ *   The kernels tile the key axis, keep a running row max and denominator, rescale the output
+ *   accumulator when the max moves, and write only O and LSE: S and P never reach memory.
+ *
+ * Visibility (bottom-right aligned, "04 · FA4 ...", section 6.2 and the section 7 table):
+ *   query row i of a sequence with Lq queries and Lk keys sits at key position p = i + Lk - Lq;
+ *   key j < Lk is visible iff  j <= p + w_right  (causal forces w_right = 0; w_right == -1 with
+ *   causal == 0 means no right bound)  and  j >= p - w_left  (w_left == -1: no left bound).
+ *   A row that sees no key gets O = 0 and LSE = -inf.
+ *
+ * Conventions shared by every call:
+ *   - All pointers marked "device" are device addresses on the current CUDA device; the caller
+ *     owns every buffer.  The library never allocates, frees or retains memory.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *     Nothing synchronises the host except attn_get_device_status().
+ *   - Tensors are dense row-major with the last dimension contiguous.  q, k, v, out, k_cache
+ *     and v_cache must be 16-byte aligned; lse 4-byte aligned; workspace 256-byte aligned.
+ *   - The library is stateless apart from a per-device status word and a per-device cache of
+ *     kernel attributes; calls from several host threads on different streams are safe.
+ *   - Errors: argument checks run before any launch and return ATTN_ERR_INVALID_ARG,
+ *     ATTN_ERR_UNSUPPORTED or ATTN_ERR_WORKSPACE without touching the device.  A failed
+ *     launch returns ATTN_ERR_CUDA.  Faults detected on the device (a wait that exceeded its
+ *     time limit, an index outside its buffer in cu_seqlens, cache_seqlens or block_table)
+ *     never trap: the kernel records a flag, skips the offending work and exits, and
+ *     attn_get_device_status() reports it.
+ */
+#ifndef ATTN_H
+#define ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = -1,    /* null pointer, bad size, misaligned buffer */
+    ATTN_ERR_UNSUPPORTED = -2,    /* valid but not built: head_dim, group size, page size */
+    ATTN_ERR_WORKSPACE = -3,      /* workspace missing or smaller than required */
+    ATTN_ERR_CUDA = -4,           /* a CUDA runtime/driver call failed */
+    ATTN_ERR_DEVICE_TIMEOUT = -5, /* a kernel wait exceeded its limit and the kernel gave up */
+    ATTN_ERR_DEVICE_BOUNDS = -6   /* a device-side index (seqlens, page ids) was out of range */
+} attn_status_t;
+
+/*
+ * attn_fwd -- varlen prefill ("flash_attn_varlen_func" in "04 · FA4 ...", sections 3-5;
+ * tiling per "Attention kernels ...", sections 三.2 and 七).
+ *
+ *   q             device bf16 [total_q, nheads_q, head_dim]; sequence b owns rows
+ *                 [cu_seqlens_q[b], cu_seqlens_q[b+1])
+ *   k, v          device bf16 [total_k, nheads_kv, head_dim]; sequence b owns rows
+ *                 [cu_seqlens_k[b], cu_seqlens_k[b+1])
+ *   out           device bf16 [total_q, nheads_q, head_dim] (written for rows inside a sequence)
+ *   lse           device fp32 [nheads_q, total_q], natural log
+ *   cu_seqlens_q, cu_seqlens_k   device int32 [batch + 1], non-decreasing, last entry
+ *                 <= total_q (resp. total_k); checked on the device (ATTN_ERR_DEVICE_BOUNDS)
+ *   batch, total_q, total_k      host sizes (the C ABI needs them to describe the tensors)
+ *   max_seqlen_q, max_seqlen_k   upper bounds on the per-sequence lengths (sizing only)
+ *   nheads_q, nheads_kv          nheads_q % nheads_kv == 0, group nheads_q/nheads_kv <= 128
+ *   head_dim      64 or 128
+ *   softmax_scale finite and > 0 (callers wanting the default pass head_dim^-0.5)
+ *   causal, window_left, window_right   see "Visibility"; window values >= -1
+ *   workspace     device scratch of at least attn_fwd_workspace_bytes(...) bytes, holding the
+ *                 tile work list; contents need not be initialised; not retained after the
+ *                 stream reaches the end of the call
+ *   stream        cudaStream_t
+ * Two calls that share a workspace must not overlap on the device.
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch,
+                       int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                       int nheads_q, int nheads_kv, int head_dim, float softmax_scale,
+                       int causal, int window_left, int window_right, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace attn_fwd needs for these sizes (0 on invalid sizes). */
+size_t attn_fwd_workspace_bytes(int batch, int max_seqlen_q, int nheads_q, int nheads_kv);
+
+/*
+ * attn_decode_kvcache -- seqlen_q = 1 decode over a paged KV cache with split-KV and an
+ * LSE-weighted combine ("flash_attn_with_kvcache" in "04 · FA4 ...", sections 6.1-6.2;
+ * "Attention kernels ...", sections 五.2, 五.3, 六.1 and 六.3).
+ *
+ *   q             device bf16 [batch, nheads_q, head_dim] (one new token per sequence)
+ *   k_cache, v_cache   device bf16 [num_pages, page_size, nheads_kv, head_dim]
+ *   cache_seqlens device int32 [batch]; sequence b attends to its keys 0 .. cache_seqlens[b]-1
+ *                 (all of them: bottom-right causal with one query); must be in
+ *                 [0, max_pages_per_seq * page_size] (checked on the device)
+ *   block_table   device int32 [batch, max_pages_per_seq]; key j of sequence b is at
+ *                 page block_table[b][j / page_size], slot j % page_size; entries past
+ *                 ceil(cache_seqlens[b] / page_size) are never read; ids must be in
+ *                 [0, num_pages) (checked on the device)
+ *   page_size     a multiple of 16 that divides 64 or is a multiple of 64
+ *   num_splits    0 = choose automatically (1..16), else 1..64; split s of sequence b covers a
+ *                 contiguous range of whole 64-key chunks; an empty split has weight 0
+ *   out           device bf16 [batch, nheads_q, head_dim]
+ *   lse           device fp32 [batch, nheads_q], natural log
+ *   batch, nheads_q, nheads_kv, head_dim, max_pages_per_seq, num_pages   host sizes;
+ *                 head_dim 64 or 128; nheads_q % nheads_kv == 0
+ *   softmax_scale finite and > 0
+ *   workspace     device scratch of attn_decode_workspace_bytes(batch, nheads_q, head_dim,
+ *                 num_splits) bytes for the split partials (may be NULL when that is 0)
+ *   stream        cudaStream_t
+ */
+attn_status_t attn_decode_kvcache(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* cache_seqlens, const int32_t* block_table,
+                                  int page_size, int num_splits, void* out, float* lse,
+                                  int batch, int nheads_q, int nheads_kv, int head_dim,
+                                  int max_pages_per_seq, int num_pages, float softmax_scale,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of split-partial workspace for attn_decode_kvcache; num_splits 0 sizes for the
+ * automatic choice (at most 16 splits).  0 when one split needs no workspace. */
+size_t attn_decode_workspace_bytes(int batch, int nheads_q, int head_dim, int num_splits);
+
+/* The split count num_splits = 0 resolves to, for these sizes on a GPU with num_sms SMs. */
+int attn_decode_num_splits(int batch, int nheads_q, int nheads_kv, int max_pages_per_seq,
+                           int page_size, int num_sms);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's status word:
+ * ATTN_ERR_DEVICE_TIMEOUT, ATTN_ERR_DEVICE_BOUNDS, ATTN_ERR_CUDA for a sticky CUDA error,
+ * else ATTN_OK.
+ */
+attn_status_t attn_get_device_status(void* stream);
+
+/* Static description of a status code. */
+const char* attn_status_string(attn_status_t status);
+
+/*
+ * Host copy of the key-block range rule the prefill kernels use ("Attention kernels ...",
+ * section 七.2-七.3; "04 · FA4 ...", section 7: n_block_min / n_block_max).  For query rows
+ * i_min..i_max (0-based within the sequence) it stores in *lo, *hi the half-open range of
+ * block_n-key blocks holding any visible key, and returns 0.  attn_kv_block_masked() returns 1
+ * when block j holds a key invisible to some row of i_min..i_max (so the kernel masks it
+ * element-wise), else 0.  Exposed so the integer work can be checked without a GPU.
+ */
+int attn_kv_block_range(int i_min, int i_max, int seqlen_q, int seqlen_k, int block_n,
+                        int causal, int window_left, int window_right, int* lo, int* hi);
+int attn_kv_block_masked(int j, int i_min, int i_max, int seqlen_q, int seqlen_k, int block_n,
+                         int causal, int window_left, int window_right);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H */

@@ -1,0 +1,155 @@
+"""CPU checks of libattn.so: it loads, exports every symbol include/attn.h declares, rejects bad
+arguments before touching a device, and its integer tile logic matches brute force over the
+oracle's visibility rule (bit-exact)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from exact_attention_70_gb300 import build as attn_build
+from exact_attention_70_gb300 import binding
+from oracle import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    attn_build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "attn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "attn_fwd" in names and "attn_decode_kvcache" in names
+    for n in names:
+        assert hasattr(lib, n), n
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code in range(-6, 1):
+        assert lib.attn_status_string(code)
+
+
+def test_workspace_sizes(lib):
+    # tile list: header + prefix + (pairs of 128-row tiles) x Hkv int4 entries
+    b = binding.attn_fwd_workspace_bytes(4, 4096, 16, 16)
+    assert b == 256 + 32 + 4 * 16 * 16 * 16
+    assert binding.attn_fwd_workspace_bytes(1, 100, 6, 4) == 0  # Hq % Hkv != 0
+    # decode partials: O fp32 + LSE fp32 per (b, h, split), 256-byte aligned pieces
+    assert binding.attn_decode_workspace_bytes(64, 32, 128, 1) == 0
+    assert binding.attn_decode_workspace_bytes(64, 32, 128, 16) == 64 * 32 * 16 * 128 * 4 + 64 * 32 * 16 * 4
+    assert binding.attn_decode_workspace_bytes(64, 32, 128, 0) == binding.attn_decode_workspace_bytes(64, 32, 128, 16)
+
+
+def test_num_splits_heuristic(lib):
+    # long sequences: one split per ~2048 keys, capped at 16
+    assert binding.attn_decode_num_splits(64, 32, 8, 128, 256, 152) == 16
+    # short sequences, few groups: enough splits for several waves of CTAs
+    s = binding.attn_decode_num_splits(1, 8, 8, 4, 256, 152)
+    assert 1 <= s <= 16 and s * 8 >= 16
+    assert binding.attn_decode_num_splits(2, 4, 4, 1, 16, 152) >= 1
+
+
+def test_bad_arguments_are_rejected_before_any_launch(lib):
+    P = ctypes.c_void_p
+    fake = P(4096)  # never dereferenced: every call below fails validation first
+    f = lib.attn_fwd
+    args = dict(q=fake, k=fake, v=fake, out=fake, lse=fake, cuq=fake, cuk=fake, batch=1,
+                tq=16, tk=16, mq=16, mk=16, hq=4, hkv=2, d=128, scale=0.1, causal=1, wl=-1,
+                wr=-1, ws=fake, wsb=1 << 20, stream=None)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return f(*a.values())
+
+    assert call(hq=6, hkv=4) == -1            # Hq % Hkv
+    assert call(d=96) == -2                   # head_dim not built
+    assert call(scale=0.0) == -1
+    assert call(scale=float("nan")) == -1
+    assert call(wl=-2) == -1
+    assert call(q=None) == -1
+    assert call(q=P(4098)) == -1              # misaligned
+    assert call(ws=None) == -3
+    assert call(wsb=16) == -3
+    assert call(batch=0) == 0                 # nothing to do
+    dec = lib.attn_decode_kvcache
+    base = [fake, fake, fake, fake, fake, 256, 0, fake, fake, 2, 8, 2, 128, 4, 8, 0.1, fake,
+            1 << 20, None]
+
+    def dcall(i, v):
+        a = list(base)
+        a[i] = v
+        return dec(*a)
+
+    assert dcall(5, 48) == -2                 # page size neither divides nor is a multiple of 64
+    assert dcall(5, 8) == -2                  # not a multiple of 16
+    assert dcall(6, 65) == -1                 # num_splits out of range
+    assert dcall(12, 80) == -2                # head_dim
+    assert dcall(10, 3) == -1                 # Hq % Hkv
+    assert dcall(0, None) == -1
+    assert dcall(9, 0) == 0                   # batch 0
+
+
+# ---- tile logic vs brute force over the oracle's visibility rule -------------------------
+
+def brute_blocks(i_min, i_max, Lq, Lk, bn, causal, wl, wr):
+    need, masked = [], []
+    nblk = (Lk + bn - 1) // bn
+    for j in range(nblk):
+        vis = [oracle.allowed(i, kk, Lq, Lk, causal, wl, wr)
+               for i in range(i_min, i_max + 1) for kk in range(j * bn, j * bn + bn)]
+        if any(vis):
+            need.append(j)
+            masked.append(not all(vis))
+    return need, masked
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_block_range_and_mask_match_brute_force(lib, seed):
+    g = torch.Generator().manual_seed(seed)
+    bn = [4, 8, 16][seed % 3]
+    for _ in range(120):
+        Lq = int(torch.randint(1, 60, (1,), generator=g))
+        Lk = int(torch.randint(0, 70, (1,), generator=g))
+        causal = bool(torch.randint(0, 2, (1,), generator=g))
+        wl = int(torch.randint(-1, 20, (1,), generator=g))
+        wr = int(torch.randint(-1, 20, (1,), generator=g))
+        i_min = int(torch.randint(0, Lq, (1,), generator=g))
+        i_max = int(torch.randint(i_min, Lq, (1,), generator=g))
+        need, masked = brute_blocks(i_min, i_max, Lq, Lk, bn, causal, wl, wr)
+        lo, hi = binding.attn_kv_block_range(i_min, i_max, Lq, Lk, bn, causal, wl, wr)
+        assert list(range(lo, hi)) == need, (Lq, Lk, causal, wl, wr, i_min, i_max)
+        got = [binding.attn_kv_block_masked(j, i_min, i_max, Lq, Lk, bn, causal, wl, wr)
+               for j in range(lo, hi)]
+        assert got == masked, (Lq, Lk, causal, wl, wr, i_min, i_max)
+
+
+def test_block_figure_from_the_library(golden):
+    ex = golden["block_masks"]
+    B, n = 4, 8
+    for key, wl in (("causal", -1), ("causal_window", 2 * B)):
+        rows = []
+        for qb in range(n):
+            lo, hi = binding.attn_kv_block_range(qb * B, qb * B + B - 1, n * B, n * B, B, True,
+                                                 wl, -1)
+            row = ""
+            for kb in range(n):
+                if not lo <= kb < hi:
+                    row += "."
+                elif not binding.attn_kv_block_masked(kb, qb * B, qb * B + B - 1, n * B, n * B,
+                                                      B, True, wl, -1):
+                    row += "F"
+                else:
+                    row += "D" if kb == qb else "E"
+            rows.append(row)
+        assert rows == ex[key]
