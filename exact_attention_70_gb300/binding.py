@@ -205,3 +205,43 @@ def attn_decode_kvcache(q, k_cache, v_cache, cache_seqlens, block_table, softmax
     if rc != 0:
         raise AttnError(rc, "attn_decode_kvcache")
     return out, lse
+
+
+def attn_decode_kvcache_noalloc(q, k_cache, v_cache, cache_seqlens, block_table,
+                                softmax_scale=None, num_splits=0, out=None, lse=None,
+                                stream=None):
+    """Decode over a paged cache without any workspace from the caller.
+
+    For callers that cannot allocate device memory: the split partials live in a 32 MiB
+    scratch array owned by the library (see attn_decode_kvcache_noalloc in include/attn.h).
+    Calls on one device share that array, so calls whose kernels overlap on the GPU race.
+    The outputs are allocated here only when `out` / `lse` are not given.
+    """
+    lib = load()
+    fn = lib.attn_decode_kvcache_noalloc
+    if fn.argtypes is None:
+        P, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        fn.restype = i32
+        fn.argtypes = [P, P, P, P, P, i32, i32, P, P, i32, i32, i32, i32, i32, i32, f32, P]
+    _check(q, "q", torch.bfloat16, 3)
+    _check(k_cache, "k_cache", torch.bfloat16, 4)
+    _check(v_cache, "v_cache", torch.bfloat16, 4)
+    _check(cache_seqlens, "cache_seqlens", torch.int32, 1)
+    _check(block_table, "block_table", torch.int32, 2)
+    batch, Hq, d = q.shape
+    num_pages, page_size, Hkv, dk = k_cache.shape
+    if v_cache.shape != k_cache.shape or dk != d:
+        raise ValueError("k_cache and v_cache must both be [num_pages, page_size, Hkv, d]")
+    scale = d ** -0.5 if softmax_scale is None else float(softmax_scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((batch, Hq), dtype=torch.float32, device=q.device)
+    _check(out, "out", torch.bfloat16, 3)
+    _check(lse, "lse", torch.float32, 2)
+    rc = fn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_seqlens), _ptr(block_table),
+            page_size, int(num_splits), _ptr(out), _ptr(lse), batch, Hq, Hkv, d,
+            block_table.shape[1], num_pages, scale, _stream(stream))
+    if rc != 0:
+        raise AttnError(rc, "attn_decode_kvcache_noalloc")
+    return out, lse

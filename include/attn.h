@@ -119,6 +119,34 @@ attn_status_t attn_decode_kvcache(const void* q, const void* k_cache, const void
                                   int max_pages_per_seq, int num_pages, float softmax_scale,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * attn_decode_kvcache_noalloc -- attn_decode_kvcache for callers that cannot allocate device
+ * memory.  The pages describe no counterpart of this call; it exists because some callers own
+ * no allocator: a plugin behind a host interface that passes tensors but no allocation hook,
+ * a server that has reserved all free HBM for its KV cache, or a latency-bound loop where
+ * cudaMalloc's possible device synchronisation is unacceptable.
+ *
+ * Arguments, layouts and results are those of attn_decode_kvcache without the workspace
+ * pair; the caller still passes every input and output.  The split partials go to a 32 MiB
+ * array of __device__ memory owned by the library (every GPU that loads the library holds it
+ * until the process exits).  A request whose partials would exceed 32 MiB, i.e.
+ * attn_decode_workspace_bytes(batch, nheads_q, head_dim, splits) > 33554432 with `splits` the
+ * resolved split count, returns ATTN_ERR_WORKSPACE and launches nothing.
+ *
+ * The first call on a device looks up the array's address on that device (that device must be
+ * current); make that first call before any stream capture.  No call allocates or frees device
+ * memory.  All calls on a device share the array and it keeps the last call's contents
+ * (nothing needs clearing: each call rewrites every slot it reads); calls whose kernels
+ * overlap on the GPU race on it, so order them on one stream or by events.
+ */
+attn_status_t attn_decode_kvcache_noalloc(const void* q, const void* k_cache,
+                                          const void* v_cache, const int32_t* cache_seqlens,
+                                          const int32_t* block_table, int page_size,
+                                          int num_splits, void* out, float* lse, int batch,
+                                          int nheads_q, int nheads_kv, int head_dim,
+                                          int max_pages_per_seq, int num_pages,
+                                          float softmax_scale, void* stream);
+
 /* Bytes of split-partial workspace for attn_decode_kvcache; num_splits 0 sizes for the
  * automatic choice (at most 16 splits).  0 when one split needs no workspace. */
 size_t attn_decode_workspace_bytes(int batch, int nheads_q, int head_dim, int num_splits);
