@@ -14,6 +14,8 @@
 //   * warp 8 issues TMA loads (Q once per item; K and V blocks into 2-stage rings);
 //   * warp 9 owns the tensor memory and issues every tcgen05.mma from one thread;
 //     S_t = Q_t K^T lands in TMEM columns [128 t, 128 t + 128), O_t in [256 + d t, ...);
+//   * warps 10-11 only complete warpgroup 2, whose registers (80 per thread) go to the
+//     softmax warpgroups (208 per thread) through setmaxnreg;
 //   * warps 0-3 (tile 0) and 4-7 (tile 1) run the online softmax, one thread per TMEM lane,
 //     i.e. one thread per query row; they write P as bf16 back over the first 64 columns of
 //     S_t, and the MMA warp reads it from there as the A operand of O_t += P V;
@@ -321,9 +323,9 @@ __device__ void fwd_mma(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32
 
 // ---- softmax / correction / epilogue (one warpgroup per Q tile, one thread per row) -------
 
-template <int D>
+template <int D, int t>
 __device__ void fwd_softmax(const FwdParams& p, FwdBars* bars, uint32_t tmem,
-                            const Watchdog& wd, int n_items, int t, int quarter, int lane) {
+                            const Watchdog& wd, int n_items, int quarter, int lane) {
     using C = FwdCfg<D>;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -352,26 +354,33 @@ __device__ void fwd_softmax(const FwdParams& p, FwdBars* bars, uint32_t tmem,
             for (int j = it.lo[t]; j < it.hi[t]; ++j) {
                 if (!__all_sync(0xffffffffu, wd.wait(&bars->s_full[t], blk & 1))) return;
                 tc_fence_after();
-                uint32_t s[4][32];
+                uint32_t s[128];
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(tS + c4 * 32, s[c4]);
+                for (int c4 = 0; c4 < 4; ++c4)
+                    tmem_ld32(tS + c4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c4 * 32]));
                 tmem_wait_ld();
                 if (kv_block_masked(j, it.imin[t], it.imax[t], it.Lq, it.Lk, kFwdBlockN,
                                     p.causal, p.wl, p.wr)) {
                     const int key0 = j * kFwdBlockN;
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4)
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            const int key = key0 + c4 * 32 + c;
-                            if (key < kmin || key > kmax) s[c4][c] = __float_as_uint(-INFINITY);
-                        }
+                    for (int c = 0; c < 128; ++c) {
+                        const int key = key0 + c;
+                        if (key < kmin || key > kmax) s[c] = __float_as_uint(-INFINITY);
+                    }
                 }
-                float mx = -INFINITY;
+                // row max: eight independent chains of 3-input max, then a short tree
+                float acc[8];
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4)
+                for (int a = 0; a < 8; ++a) {
+                    float m = __uint_as_float(s[a]);
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(s[c4][c]));
+                    for (int i = 1; i < 15; i += 2)
+                        m = fmax3(m, __uint_as_float(s[a + 8 * i]),
+                                  __uint_as_float(s[a + 8 * (i + 1)]));
+                    acc[a] = fmaxf(m, __uint_as_float(s[a + 120]));
+                }
+                const float mx = fmaxf(fmax3(acc[0], acc[1], acc[2]),
+                                       fmax3(fmax3(acc[3], acc[4], acc[5]), acc[6], acc[7]));
                 const float m_blk = mx * sl2;
                 const bool need = m_blk > m_run + kRescaleThreshold;
                 const float m_new = need ? m_blk : m_run;
@@ -379,21 +388,33 @@ __device__ void fwd_softmax(const FwdParams& p, FwdBars* bars, uint32_t tmem,
                 l_run *= alpha;
                 m_run = m_new;
                 const float mref = (m_run == -INFINITY) ? 0.f : m_run;
-                float sum = 0.f;
+                // P = exp2(s * scale*log2e - m): paired FFMA, MUFU ex2, paired sums
+                const uint64_t sl2x2 = f2_make(sl2, sl2);
+                const uint64_t negm2 = f2_make(-mref, -mref);
+                uint64_t sum2[4] = {0, 0, 0, 0};
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const int c = h * 64 + 2 * e;
-                        const float p0 =
-                            ex2_approx(fmaf(__uint_as_float(s[c >> 5][c & 31]), sl2, -mref));
-                        const float p1 = ex2_approx(
-                            fmaf(__uint_as_float(s[(c + 1) >> 5][(c + 1) & 31]), sl2, -mref));
-                        sum += p0 + p1;
+                        const uint64_t x2 = f2_fma(
+                            f2_make(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2,
+                            negm2);
+                        float x0, x1;
+                        f2_split(x2, x0, x1);
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        sum2[e & 3] = f2_add(sum2[e & 3], f2_make(p0, p1));
                         pk[e] = pack_bf16x2(p0, p1);
                     }
                     tmem_st32(tS + h * 32, pk);
+                }
+                float sum;
+                {
+                    const uint64_t t2 = f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3]));
+                    float lo, hi;
+                    f2_split(t2, lo, hi);
+                    sum = lo + hi;
                 }
                 l_run += sum;
                 if (__any_sync(0xffffffffu, need) && j > it.lo[t]) {
@@ -495,17 +516,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     const Watchdog wd{&bars->abort_flag, p.status};
     const int n_items = p.header->n_items;
 
-    if (warp == 8) {
-        if (lane == 0) fwd_producer<D>(p, smem, bars, wd, n_items);
-    } else if (warp == 9) {
-        if (lane == 0) {
-            fwd_mma<D>(p, smem, bars, tmem, wd, n_items);
-            // every tcgen05 op this thread issued has finished before TMEM is released
-            umma_commit(&bars->drain);
-            drain_wait(&bars->drain, 0);
+    // Registers: launched at 168 per thread (384 threads); warpgroup 2 (TMA, MMA, 2 idle
+    // warps) drops to 80 and the two softmax warpgroups rise to 208:
+    // 128 * 80 + 256 * 208 = 63488 <= 384 * 168 = 64512.
+    if (warp >= 8) {
+        regs_decrease<80>();
+        if (warp == 8) {
+            if (lane == 0) fwd_producer<D>(p, smem, bars, wd, n_items);
+        } else if (warp == 9) {
+            if (lane == 0) {
+                fwd_mma<D>(p, smem, bars, tmem, wd, n_items);
+                // every tcgen05 op this thread issued has finished before TMEM is released
+                umma_commit(&bars->drain);
+                drain_wait(&bars->drain, 0);
+            }
         }
     } else {
-        fwd_softmax<D>(p, bars, tmem, wd, n_items, warp >> 2, warp & 3, lane);
+        regs_increase<208>();
+        if (warp < 4)
+            fwd_softmax<D, 0>(p, bars, tmem, wd, n_items, warp & 3, lane);
+        else
+            fwd_softmax<D, 1>(p, bars, tmem, wd, n_items, warp & 3, lane);
     }
     __syncwarp();
     tc_fence_before();
