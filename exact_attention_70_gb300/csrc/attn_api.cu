@@ -9,7 +9,7 @@
 #include <stdint.h>
 #include <string.h>
 
-#include "../../include/attn.h"
+#include "attn.h"
 #include "kernels.h"
 #include "tile_math.h"
 

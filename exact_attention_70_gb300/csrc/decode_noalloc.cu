@@ -24,7 +24,7 @@
 #include <mutex>
 #include <stdint.h>
 
-#include "../../include/attn.h"
+#include "attn.h"
 
 namespace {
 
