@@ -11,17 +11,20 @@
 //   * a work item is two 128-row Q tiles of one (sequence, kv head); its rows pack
 //     tokens x the g query heads of that kv head (pack_gqa), so each K/V block is loaded once
 //     for 256 query rows;
-//   * warp 8 issues TMA loads (Q once per item; K and V blocks into 2-stage rings);
-//   * warp 9 owns the tensor memory and issues every tcgen05.mma from one thread;
-//     S_t = Q_t K^T lands in TMEM columns [128 t, 128 t + 128), O_t in [256 + d t, ...);
-//   * warps 10-11 only complete warpgroup 2, whose registers (80 per thread) go to the
-//     softmax warpgroups (208 per thread) through setmaxnreg;
+//   * warp 8 issues TMA loads: Q once per item, then the item's K and V blocks through one
+//     ring of shared-memory slots, in the order the tensor core consumes them
+//     (K_0, K_1, V_0, K_2, V_1, ..., V_{m-1});
+//   * warp 9 issues every S_t = Q_t K^T (fp32 into TMEM columns [128 t, 128 t + 128)) and
+//     warp 10 every O_t += P_t V (O_t in TMEM columns [256 + d t, ...)), both with operands in
+//     shared memory.  An issuing thread blocks until the tensor pipe accepts each instruction
+//     and the pipe holds little beyond the one executing, so a wait between two groups on a
+//     single issuer idles the tensor cores; with two issuers one thread's waits overlap the
+//     other thread's MMAs;
 //   * warps 0-3 (tile 0) and 4-7 (tile 1) run the online softmax, one thread per TMEM lane,
-//     i.e. one thread per query row; they write P as bf16 back over the first 64 columns of
-//     S_t, and the MMA warp reads it from there as the A operand of O_t += P V;
-//   * the MMA warp issues, per tile, PV_t(j) and then S_t(j+1) once PV_t(j) has completed
-//     (S_t(j+1) overwrites the columns PV_t(j) reads), alternating between the two tiles so
-//     one tile's softmax overlaps the other tile's MMAs;
+//     i.e. one thread per query row.  They release S_t as soon as it is in registers, so
+//     S_t(j+1) is computed while they exponentiate block j, and write P_t as bf16 to shared
+//     memory in the 128-byte-swizzled K-major layout the tensor core reads as the A operand;
+//   * warps 8-11 (warpgroup 2) give registers to the softmax warpgroups through setmaxnreg;
 //   * the running max only moves the accumulator's reference when it grows by more than
 //     2^8 (the result is exact for any reference; this only bounds P <= 256), so the O
 //     rescale through TMEM is rare after the first blocks.
@@ -44,28 +47,29 @@ struct FwdCfg {
     static constexpr int kAtomBytes = 128 * 128;           // 128 rows x 128 B
     static constexpr int kQTile = kHalves * kAtomBytes;    // one 128-row Q tile
     static constexpr int kKvTile = kHalves * kAtomBytes;   // one 128-key K or V block
-    static constexpr int kNK = D == 128 ? 2 : 4;           // K ring stages
-    static constexpr int kNV = D == 128 ? 2 : 4;           // V ring stages
+    static constexpr int kPTile = 2 * kAtomBytes;          // 128 rows x 128 keys of P, bf16
+    static constexpr int kSlots = D == 128 ? 3 : 8;        // K/V ring slots
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kFwdTilesPerItem * kQTile;
-    static constexpr int kOffV = kOffK + kNK * kKvTile;
-    static constexpr int kOffBar = kOffV + kNV * kKvTile;
-    static constexpr int kSmem = kOffBar + 1024 + 1024;    // barriers + alignment slack
+    static constexpr int kOffP = kOffQ + kFwdTilesPerItem * kQTile;
+    static constexpr int kOffKV = kOffP + kFwdTilesPerItem * kPTile;
+    static constexpr int kOffBar = kOffKV + kSlots * kKvTile;
+    static constexpr int kSmem = kOffBar + 512 + 1024;     // barriers + alignment slack
+    static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
     static constexpr uint32_t kTmemCols = 512;
-    // TMEM columns: S_t (fp32, later P_t as bf16 pairs) and O_t
+    // TMEM columns of S_t (fp32) and O_t (fp32)
     __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
     __device__ static constexpr uint32_t col_o(int t) { return 256u + D * t; }
 };
 
 struct FwdBars {
     uint64_t q_full, q_empty;
-    uint64_t k_full[4], k_empty[4];
-    uint64_t v_full[4], v_empty[4];
-    uint64_t s_full[2], p_full[2], pv_done[2], o_free[2];
-    uint64_t drain;
+    uint64_t kv_full[8], kv_empty[8];
+    uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_free[2];
+    uint64_t drain[2];
     uint32_t tmem_base;
     int abort_flag;
 };
+static_assert(sizeof(FwdBars) <= 512, "barrier block");
 
 // Geometry of one work item, derived identically by every role.
 struct Item {
@@ -113,6 +117,19 @@ __device__ __forceinline__ Item load_item(const FwdParams& p, int idx) {
     return it;
 }
 
+__device__ __forceinline__ bool tile_uses(const Item& it, int t, int j) {
+    return it.mma[t] && it.lo[t] <= j && j < it.hi[t];
+}
+
+// Positions in the K/V ring, relative to the item's first slot, of K_i and V_i for an item of
+// m key blocks.  The two tiles' key ranges overlap or touch, so their union [jlo, jhi) has no
+// gap; the producer fills 2m slots in the order K_0, K_1, V_0, K_2, V_1, ..., K_{m-1},
+// V_{m-2}, V_{m-1}.
+__device__ __forceinline__ uint32_t ring_pos_k(int i) { return i == 0 ? 0u : 2u * i - 1u; }
+__device__ __forceinline__ uint32_t ring_pos_v(int i, int m) {
+    return i == m - 1 ? 2u * m - 1u : 2u * i + 2u;
+}
+
 // Persistent schedule: round k hands CTA c the item k*G + c (even rounds) or
 // k*G + G-1-c (odd rounds); the list is sorted longest-first, so the snake order evens out
 // the per-CTA totals.
@@ -134,7 +151,7 @@ __device__ void drain_wait(uint64_t* bar, uint32_t parity) {
 template <int D>
 __device__ void fwd_producer_loop(const FwdParams& p, uint8_t* smem, FwdBars* bars,
                                   const Watchdog& wd, int n_items, uint32_t& q_cnt,
-                                  uint32_t& k_cnt, uint32_t& v_cnt) {
+                                  uint32_t& kv_cnt) {
     using C = FwdCfg<D>;
     tma_prefetch_desc(&p.tm_q);
     tma_prefetch_desc(&p.tm_k);
@@ -161,30 +178,25 @@ __device__ void fwd_producer_loop(const FwdParams& p, uint8_t* smem, FwdBars* ba
                             &bars->q_full, h * 64, it.kvh * p.g, it.q0 + it.tok0[t]);
         }
         ++q_cnt;
-        for (int j = it.jlo; j < it.jhi; ++j) {
-            {
-                const uint32_t st = k_cnt % C::kNK;
-                if (k_cnt >= C::kNK && !wd.wait(&bars->k_empty[st], ((k_cnt / C::kNK) - 1) & 1))
-                    return;
-                mbar_arrive_expect_tx(&bars->k_full[st], C::kKvTile);
+        const int m = it.jhi - it.jlo;
+        for (int r = 0; r < 2 * m; ++r) {
+            // inverse of ring_pos_k / ring_pos_v
+            const bool last = r == 2 * m - 1;
+            const bool is_v = last || (r > 0 && (r & 1) == 0);
+            const int i = is_v ? (last ? m - 1 : (r - 2) / 2) : (r + 1) / 2;
+            const uint32_t n = kv_cnt + r;
+            const uint32_t st = n % C::kSlots;
+            if (n >= C::kSlots && !wd.wait(&bars->kv_empty[st], ((n / C::kSlots) - 1) & 1))
+                return;
+            mbar_arrive_expect_tx(&bars->kv_full[st], C::kKvTile);
+            const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
 #pragma unroll
-                for (int h = 0; h < C::kHalves; ++h)
-                    tma_load_3d(smem + C::kOffK + st * C::kKvTile + h * C::kAtomBytes, &p.tm_k,
-                                &bars->k_full[st], h * 64, it.kvh, it.k0 + j * kFwdBlockN);
-                ++k_cnt;
-            }
-            {
-                const uint32_t st = v_cnt % C::kNV;
-                if (v_cnt >= C::kNV && !wd.wait(&bars->v_empty[st], ((v_cnt / C::kNV) - 1) & 1))
-                    return;
-                mbar_arrive_expect_tx(&bars->v_full[st], C::kKvTile);
-#pragma unroll
-                for (int h = 0; h < C::kHalves; ++h)
-                    tma_load_3d(smem + C::kOffV + st * C::kKvTile + h * C::kAtomBytes, &p.tm_v,
-                                &bars->v_full[st], h * 64, it.kvh, it.k0 + j * kFwdBlockN);
-                ++v_cnt;
-            }
+            for (int h = 0; h < C::kHalves; ++h)
+                tma_load_3d(smem + C::kOffKV + st * C::kKvTile + h * C::kAtomBytes, map,
+                            &bars->kv_full[st], h * 64, it.kvh,
+                            it.k0 + (it.jlo + i) * kFwdBlockN);
         }
+        kv_cnt += 2 * m;
     }
 }
 
@@ -192,31 +204,28 @@ template <int D>
 __device__ void fwd_producer(const FwdParams& p, uint8_t* smem, FwdBars* bars,
                              const Watchdog& wd, int n_items) {
     using C = FwdCfg<D>;
-    uint32_t q_cnt = 0, k_cnt = 0, v_cnt = 0;
-    fwd_producer_loop<D>(p, smem, bars, wd, n_items, q_cnt, k_cnt, v_cnt);
-    // Every stage holds at most one load in flight: wait for the latest load of each one.
+    uint32_t q_cnt = 0, kv_cnt = 0;
+    fwd_producer_loop<D>(p, smem, bars, wd, n_items, q_cnt, kv_cnt);
+    // Every slot holds at most one load in flight: wait for the latest load of each one.
     if (q_cnt > 0) drain_wait(&bars->q_full, (q_cnt - 1) & 1);
-    for (uint32_t st = 0; st < C::kNK && st < k_cnt; ++st)
-        drain_wait(&bars->k_full[st], ((k_cnt - 1 - st) / C::kNK) & 1);
-    for (uint32_t st = 0; st < C::kNV && st < v_cnt; ++st)
-        drain_wait(&bars->v_full[st], ((v_cnt - 1 - st) / C::kNV) & 1);
+    for (uint32_t st = 0; st < C::kSlots && st < kv_cnt; ++st)
+        drain_wait(&bars->kv_full[st], ((kv_cnt - 1 - st) / C::kSlots) & 1);
 }
 
-// ---- MMA issuer (one thread) ---------------------------------------------------------------
+// ---- MMA issuers: warp 9 issues S = Q K^T, warp 10 issues O += P V (one thread each) ------
 
+// S_t(j) for every (j, t) of every item.  S_t(j) overwrites the TMEM columns of S_t(j-1), so
+// it waits for tile t's softmax to have read them (s_free).
 template <int D>
-__device__ void fwd_mma(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32_t tmem,
-                        const Watchdog& wd, int n_items) {
+__device__ void fwd_mma_s(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32_t tmem,
+                          const Watchdog& wd, int n_items) {
     using C = FwdCfg<D>;
-    constexpr uint32_t kIdescS = idesc_bf16_f32(128, kFwdBlockN, false, false);
-    constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
+    constexpr uint32_t kIdesc = idesc_bf16_f32(128, kFwdBlockN, false, false);
     const uint32_t q_base = smem_u32(smem + C::kOffQ);
-    const uint32_t k_base = smem_u32(smem + C::kOffK);
-    const uint32_t v_base = smem_u32(smem + C::kOffV);
+    const uint32_t kv_base = smem_u32(smem + C::kOffKV);
     const int G = gridDim.x, cta = blockIdx.x;
-    uint32_t q_cnt = 0, k_cnt = 0, v_cnt = 0;
-    uint32_t pv_cnt[2] = {0, 0};   // PV_t issued so far (== P_t consumed)
-    uint32_t o_items[2] = {0, 0};  // items in which tile t accumulated into O_t
+    uint32_t q_cnt = 0, kv_cnt = 0;
+    uint32_t s_cnt0 = 0, s_cnt1 = 0;  // S_t issued so far
     for (int k = 0; k * G < n_items; ++k) {
         const int idx = item_index(k, cta, G);
         if (idx >= n_items) continue;
@@ -224,113 +233,130 @@ __device__ void fwd_mma(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32
         if (!it.any) continue;
         if (!wd.wait(&bars->q_full, q_cnt & 1)) return;
         ++q_cnt;
-        tc_fence_after();
-        int nS[2], nPV[2];
-        bool first_pv[2] = {true, true};
-#pragma unroll
-        for (int t = 0; t < 2; ++t) nS[t] = nPV[t] = it.lo[t];
-        bool q_released = false;
-        unsigned long long t_idle = 0;
-        uint32_t idle_spins = 0;
-        while (true) {
-            bool done = true, progress = false;
+        const int m = it.jhi - it.jlo;
+        for (int i = 0; i < m; ++i) {
+            const int j = it.jlo + i;
+            const uint32_t n = kv_cnt + ring_pos_k(i);
+            const uint32_t st = n % C::kSlots;
+            if (!wd.wait(&bars->kv_full[st], (n / C::kSlots) & 1)) return;
+            const uint32_t kb = kv_base + st * C::kKvTile;
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-                if (!it.mma[t]) continue;
-                const int t2 = 1 - t;
-                if (nPV[t] < it.hi[t]) done = false;
-                // S_t(j) = Q_t K_j^T: needs K_j and the completion of PV_t(j-1), which reads P
-                // from the columns S_t(j) overwrites.
-                if (nS[t] < it.hi[t] && nS[t] == nPV[t]) {
-                    const int j = nS[t];
-                    const uint32_t n = k_cnt + (j - it.jlo);
-                    const uint32_t st = n % C::kNK;
-                    if (mbar_test(&bars->k_full[st], (n / C::kNK) & 1) &&
-                        (pv_cnt[t] == 0 || mbar_test(&bars->pv_done[t], (pv_cnt[t] - 1) & 1))) {
-                        tc_fence_after();
-                        const uint32_t qa = q_base + t * C::kQTile;
-                        const uint32_t kb = k_base + st * C::kKvTile;
+                if (!tile_uses(it, t, j)) continue;
+                uint32_t& sc = t ? s_cnt1 : s_cnt0;
+                if (sc > 0 && !wd.wait(&bars->s_free[t], (sc - 1) & 1)) return;
+                tc_fence_after();
+                const uint32_t qa = q_base + t * C::kQTile;
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk >> 2) * C::kAtomBytes + (kk & 3) * 32;
-                            umma_ss(tmem + C::col_s(t), sdesc_sw128(qa + off, 16, 1024),
-                                    sdesc_sw128(kb + off, 16, 1024), kIdescS, kk > 0);
-                        }
-                        umma_commit(&bars->s_full[t]);
-                        ++nS[t];
-                        const bool other_needs =
-                            it.mma[t2] && it.lo[t2] <= j && j < it.hi[t2] && nS[t2] <= j;
-                        if (!other_needs) umma_commit(&bars->k_empty[st]);
-                        if (!q_released && (!it.mma[0] || nS[0] == it.hi[0]) &&
-                            (!it.mma[1] || nS[1] == it.hi[1])) {
-                            umma_commit(&bars->q_empty);
-                            q_released = true;
-                        }
-                        progress = true;
-                    }
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::kAtomBytes + (kk & 3) * 32;
+                    umma_ss(tmem + C::col_s(t), sdesc_sw128(qa + off, 16, 1024),
+                            sdesc_sw128(kb + off, 16, 1024), kIdesc, kk > 0);
                 }
-                // O_t (+)= P_t(j) V_j: needs P_t(j), V_j and, for the item's first block, the
-                // previous item's epilogue to have read O_t.
-                if (nPV[t] < nS[t]) {
-                    const int j = nPV[t];
-                    const uint32_t n = v_cnt + (j - it.jlo);
-                    const uint32_t st = n % C::kNV;
-                    const bool o_ok = !first_pv[t] || o_items[t] == 0 ||
-                                      mbar_test(&bars->o_free[t], (o_items[t] - 1) & 1);
-                    if (o_ok && mbar_test(&bars->p_full[t], pv_cnt[t] & 1) &&
-                        mbar_test(&bars->v_full[st], (n / C::kNV) & 1)) {
-                        tc_fence_after();
-                        const uint32_t vb = v_base + st * C::kKvTile;
-#pragma unroll
-                        for (int kk = 0; kk < kFwdBlockN / 16; ++kk) {
-                            umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8,
-                                    sdesc_sw128(vb + kk * 16 * 128, C::kAtomBytes, 1024),
-                                    kIdescO, (first_pv[t] && kk == 0) ? 0u : 1u);
-                        }
-                        umma_commit(&bars->pv_done[t]);
-                        ++pv_cnt[t];
-                        first_pv[t] = false;
-                        ++nPV[t];
-                        const bool other_needs =
-                            it.mma[t2] && it.lo[t2] <= j && j < it.hi[t2] && nPV[t2] <= j;
-                        if (!other_needs) umma_commit(&bars->v_empty[st]);
-                        progress = true;
-                    }
-                }
+                umma_commit(&bars->s_full[t]);
+                ++sc;
             }
-            if (done) break;
-            if (progress) {
-                idle_spins = 0;
-            } else if ((++idle_spins & 63u) == 0) {
-                if (wd.aborted()) return;
-                const unsigned long long now = global_ns();
-                if (t_idle == 0) {
-                    t_idle = now;
-                } else if (now - t_idle > kWaitLimitNs) {
-                    wd.fail();
-                    return;
-                }
-            }
-            if (progress) t_idle = 0;
+            umma_commit(&bars->kv_empty[st]);  // both tiles' S_t(j) have read K_j
         }
+        umma_commit(&bars->q_empty);
+        kv_cnt += 2 * m;
+    }
+}
+
+// O_t (+)= P_t(j) V_j for every (j, t) of every item, P_t from shared memory.  The item's
+// first PV_t overwrites O_t, so it first waits for the previous item's epilogue to have read
+// O_t (o_free).
+template <int D>
+__device__ void fwd_mma_pv(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32_t tmem,
+                           const Watchdog& wd, int n_items) {
+    using C = FwdCfg<D>;
+    constexpr uint32_t kIdesc = idesc_bf16_f32(128, D, false, true);
+    const uint32_t p_base = smem_u32(smem + C::kOffP);
+    const uint32_t kv_base = smem_u32(smem + C::kOffKV);
+    const int G = gridDim.x, cta = blockIdx.x;
+    uint32_t kv_cnt = 0;
+    uint32_t pv_cnt0 = 0, pv_cnt1 = 0;    // PV_t issued so far (== P_t consumed)
+    uint32_t o_items0 = 0, o_items1 = 0;  // items in which tile t accumulated into O_t
+    for (int k = 0; k * G < n_items; ++k) {
+        const int idx = item_index(k, cta, G);
+        if (idx >= n_items) continue;
+        const Item it = load_item(p, idx);
+        if (!it.any) continue;
+        bool first0 = true, first1 = true;
+        const int m = it.jhi - it.jlo;
+        for (int i = 0; i < m; ++i) {
+            const int j = it.jlo + i;
+            const uint32_t n = kv_cnt + ring_pos_v(i, m);
+            const uint32_t st = n % C::kSlots;
+            if (!wd.wait(&bars->kv_full[st], (n / C::kSlots) & 1)) return;
+            const uint32_t vb = kv_base + st * C::kKvTile;
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
-            if (it.mma[t]) ++o_items[t];
-        k_cnt += it.jhi - it.jlo;
-        v_cnt += it.jhi - it.jlo;
+            for (int t = 0; t < 2; ++t) {
+                if (!tile_uses(it, t, j)) continue;
+                bool& first = t ? first1 : first0;
+                const uint32_t oi = t ? o_items1 : o_items0;
+                if (first && oi > 0 && !wd.wait(&bars->o_free[t], (oi - 1) & 1)) return;
+                uint32_t& pc = t ? pv_cnt1 : pv_cnt0;
+                if (!wd.wait(&bars->p_full[t], pc & 1)) return;
+                tc_fence_after();
+                const uint32_t pa = p_base + t * C::kPTile;
+#pragma unroll
+                for (int kk = 0; kk < kFwdBlockN / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::kAtomBytes + (kk & 3) * 32;
+                    umma_ss(tmem + C::col_o(t), sdesc_sw128(pa + off, 16, 1024),
+                            sdesc_sw128(vb + kk * 16 * 128, C::kAtomBytes, 1024), kIdesc,
+                            (first && kk == 0) ? 0u : 1u);
+                }
+                umma_commit(&bars->pv_done[t]);
+                ++pc;
+                first = false;
+            }
+            umma_commit(&bars->kv_empty[st]);  // both tiles' PV_t(j) have read V_j
+        }
+        if (it.mma[0]) ++o_items0;
+        if (it.mma[1]) ++o_items1;
+        kv_cnt += 2 * m;
     }
 }
 
 // ---- softmax / correction / epilogue (one warpgroup per Q tile, one thread per row) -------
 
-template <int D, int t>
-__device__ void fwd_softmax(const FwdParams& p, FwdBars* bars, uint32_t tmem,
-                            const Watchdog& wd, int n_items, int quarter, int lane) {
+// One Q tile's view of an item (the tile index is a run-time value: both softmax warpgroups
+// run the same instruction stream, which keeps the instruction cache shared between them).
+struct TileView {
+    bool rows, mma;
+    int tok0, imin, imax, lo, hi;
+};
+
+__device__ __forceinline__ TileView tile_view(const Item& it, int t) {
+    TileView v;
+    v.rows = t ? it.rows[1] : it.rows[0];
+    v.mma = t ? it.mma[1] : it.mma[0];
+    v.tok0 = t ? it.tok0[1] : it.tok0[0];
+    v.imin = t ? it.imin[1] : it.imin[0];
+    v.imax = t ? it.imax[1] : it.imax[0];
+    v.lo = t ? it.lo[1] : it.lo[0];
+    v.hi = t ? it.hi[1] : it.hi[0];
+    return v;
+}
+
+template <int D>
+__device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32_t tmem,
+                            const Watchdog& wd, int n_items, int t, int quarter, int lane) {
     using C = FwdCfg<D>;
+    uint64_t* const s_full = &bars->s_full[t];
+    uint64_t* const s_free = &bars->s_free[t];
+    uint64_t* const p_full = &bars->p_full[t];
+    uint64_t* const pv_done = &bars->pv_done[t];
+    uint64_t* const o_free = &bars->o_free[t];
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::col_s(t);
     const uint32_t tO = tmem + lane_off + C::col_o(t);
+    // This row of P_t: keys [64 a, 64 a + 64) in swizzle atom a; 16-byte unit u of the row's
+    // 128 bytes sits at unit u ^ (row % 8).
+    const uint32_t p_row = smem_u32(smem + C::kOffP + t * C::kPTile) + row * 128;
+    const uint32_t r7 = row & 7;
     const float sl2 = p.scale_log2;
     const int G = gridDim.x, cta = blockIdx.x;
     const int g = p.g;
@@ -341,8 +367,9 @@ __device__ void fwd_softmax(const FwdParams& p, FwdBars* bars, uint32_t tmem,
         const int idx = item_index(k, cta, G);
         if (idx >= n_items) continue;
         const Item it = load_item(p, idx);
-        if (!it.rows[t]) continue;
-        const int tok = it.tok0[t] + row_tok;
+        const TileView tv = tile_view(it, t);
+        if (!tv.rows) continue;
+        const int tok = tv.tok0 + row_tok;
         const bool valid = row_in_tile && tok < it.Lq;
         const int head = it.kvh * g + row_head;
         int kmin, kmax;
@@ -350,17 +377,21 @@ __device__ void fwd_softmax(const FwdParams& p, FwdBars* bars, uint32_t tmem,
         float m_run = -INFINITY, l_run = 0.f;
         __nv_bfloat16* orow =
             p.out + (static_cast<size_t>(it.q0 + tok) * p.Hq + head) * D;
-        if (it.mma[t]) {
-            for (int j = it.lo[t]; j < it.hi[t]; ++j) {
-                if (!__all_sync(0xffffffffu, wd.wait(&bars->s_full[t], blk & 1))) return;
+        if (tv.mma) {
+            for (int j = tv.lo; j < tv.hi; ++j) {
+                if (!__all_sync(0xffffffffu, wd.wait(s_full, blk & 1))) return;
                 tc_fence_after();
                 uint32_t s[128];
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4)
                     tmem_ld32(tS + c4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c4 * 32]));
                 tmem_wait_ld();
-                if (kv_block_masked(j, it.imin[t], it.imax[t], it.Lq, it.Lk, kFwdBlockN,
-                                    p.causal, p.wl, p.wr)) {
+                // S_t is in registers: the tensor core may overwrite it with S_t(j+1)
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_free);
+                if (kv_block_masked(j, tv.imin, tv.imax, it.Lq, it.Lk, kFwdBlockN, p.causal,
+                                    p.wl, p.wr)) {
                     const int key0 = j * kFwdBlockN;
 #pragma unroll
                     for (int c = 0; c < 128; ++c) {
@@ -392,22 +423,17 @@ __device__ void fwd_softmax(const FwdParams& p, FwdBars* bars, uint32_t tmem,
                 const uint64_t sl2x2 = f2_make(sl2, sl2);
                 const uint64_t negm2 = f2_make(-mref, -mref);
                 uint64_t sum2[4] = {0, 0, 0, 0};
+                uint32_t pk[64];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int c = h * 64 + 2 * e;
-                        const uint64_t x2 = f2_fma(
-                            f2_make(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2,
-                            negm2);
-                        float x0, x1;
-                        f2_split(x2, x0, x1);
-                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                        sum2[e & 3] = f2_add(sum2[e & 3], f2_make(p0, p1));
-                        pk[e] = pack_bf16x2(p0, p1);
-                    }
-                    tmem_st32(tS + h * 32, pk);
+                for (int e = 0; e < 64; ++e) {
+                    const uint64_t x2 = f2_fma(
+                        f2_make(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])),
+                        sl2x2, negm2);
+                    float x0, x1;
+                    f2_split(x2, x0, x1);
+                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                    sum2[e & 3] = f2_add(sum2[e & 3], f2_make(p0, p1));
+                    pk[e] = pack_bf16x2(p0, p1);
                 }
                 float sum;
                 {
@@ -417,11 +443,13 @@ __device__ void fwd_softmax(const FwdParams& p, FwdBars* bars, uint32_t tmem,
                     sum = lo + hi;
                 }
                 l_run += sum;
-                if (__any_sync(0xffffffffu, need) && j > it.lo[t]) {
-                    // O_t holds PV_t(j-1); it completed before S_t(j) was issued.
-                    if (!__all_sync(0xffffffffu, wd.wait(&bars->pv_done[t], (blk - 1) & 1)))
-                        return;
+                // PV_t of the previous block has finished reading P_t from shared memory and
+                // accumulating into O_t.
+                if (blk > 0) {
+                    if (!__all_sync(0xffffffffu, wd.wait(pv_done, (blk - 1) & 1))) return;
                     tc_fence_after();
+                }
+                if (__any_sync(0xffffffffu, need) && j > tv.lo) {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t o[32];
@@ -432,15 +460,20 @@ __device__ void fwd_softmax(const FwdParams& p, FwdBars* bars, uint32_t tmem,
                             o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
                         tmem_st32(tO + c * 32, o);
                     }
+                    tmem_wait_st();
+                    tc_fence_before();
                 }
-                tmem_wait_st();
-                tc_fence_before();
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    st_shared_v4(p_row + (u >> 3) * C::kAtomBytes + ((((u & 7) ^ r7)) << 4),
+                                 pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->p_full[t]);
+                if (lane == 0) mbar_arrive(p_full);
                 ++blk;
             }
             // Epilogue: O / l from TMEM, bf16, straight to global memory.
-            if (!__all_sync(0xffffffffu, wd.wait(&bars->pv_done[t], (blk - 1) & 1))) return;
+            if (!__all_sync(0xffffffffu, wd.wait(pv_done, (blk - 1) & 1))) return;
             tc_fence_after();
             const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
@@ -467,7 +500,7 @@ __device__ void fwd_softmax(const FwdParams& p, FwdBars* bars, uint32_t tmem,
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->o_free[t]);
+            if (lane == 0) mbar_arrive(o_free);
         } else if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
@@ -492,19 +525,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
         mbar_init(&bars->q_empty, 1);
-        for (int i = 0; i < 4; ++i) {
-            mbar_init(&bars->k_full[i], 1);
-            mbar_init(&bars->k_empty[i], 1);
-            mbar_init(&bars->v_full[i], 1);
-            mbar_init(&bars->v_empty[i], 1);
+        for (int i = 0; i < C::kSlots; ++i) {
+            mbar_init(&bars->kv_full[i], 1);
+            mbar_init(&bars->kv_empty[i], 1);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&bars->s_full[t], 1);
+            mbar_init(&bars->s_free[t], 4);
             mbar_init(&bars->p_full[t], 4);
             mbar_init(&bars->pv_done[t], 1);
             mbar_init(&bars->o_free[t], 4);
+            mbar_init(&bars->drain[t], 1);
         }
-        mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
         mbar_fence_init();
     }
@@ -516,27 +548,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     const Watchdog wd{&bars->abort_flag, p.status};
     const int n_items = p.header->n_items;
 
-    // Registers: launched at 168 per thread (384 threads); warpgroup 2 (TMA, MMA, 2 idle
-    // warps) drops to 80 and the two softmax warpgroups rise to 208:
+    // Registers: launched at 168 per thread (384 threads); warpgroup 2 (TMA, two MMA issuers,
+    // one idle warp) drops to 80 and the two softmax warpgroups rise to 208:
     // 128 * 80 + 256 * 208 = 63488 <= 384 * 168 = 64512.
     if (warp >= 8) {
         regs_decrease<80>();
         if (warp == 8) {
             if (lane == 0) fwd_producer<D>(p, smem, bars, wd, n_items);
-        } else if (warp == 9) {
+        } else if (warp == 9 || warp == 10) {
             if (lane == 0) {
-                fwd_mma<D>(p, smem, bars, tmem, wd, n_items);
+                if (warp == 9)
+                    fwd_mma_s<D>(p, smem, bars, tmem, wd, n_items);
+                else
+                    fwd_mma_pv<D>(p, smem, bars, tmem, wd, n_items);
                 // every tcgen05 op this thread issued has finished before TMEM is released
-                umma_commit(&bars->drain);
-                drain_wait(&bars->drain, 0);
+                umma_commit(&bars->drain[warp - 9]);
+                drain_wait(&bars->drain[warp - 9], 0);
             }
         }
     } else {
         regs_increase<208>();
-        if (warp < 4)
-            fwd_softmax<D, 0>(p, bars, tmem, wd, n_items, warp & 3, lane);
-        else
-            fwd_softmax<D, 1>(p, bars, tmem, wd, n_items, warp & 3, lane);
+        fwd_softmax<D>(p, smem, bars, tmem, wd, n_items, warp >> 2, warp & 3, lane);
     }
     __syncwarp();
     tc_fence_before();
