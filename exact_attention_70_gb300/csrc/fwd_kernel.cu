@@ -221,8 +221,11 @@ __device__ void fwd_mma_s(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint
                           const Watchdog& wd, int n_items) {
     using C = FwdCfg<D>;
     constexpr uint32_t kIdesc = idesc_bf16_f32(128, kFwdBlockN, false, false);
-    const uint32_t q_base = smem_u32(smem + C::kOffQ);
-    const uint32_t kv_base = smem_u32(smem + C::kOffKV);
+    // K-major operand descriptors (128-byte swizzle, 8-row groups 1024 B apart), as halves
+    const uint64_t dq = sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
+    const uint64_t dkv = sdesc_sw128(smem_u32(smem + C::kOffKV), 16, 1024);
+    const uint32_t q_lo = static_cast<uint32_t>(dq), d_hi = static_cast<uint32_t>(dq >> 32);
+    const uint32_t kv_lo = static_cast<uint32_t>(dkv);
     const int G = gridDim.x, cta = blockIdx.x;
     uint32_t q_cnt = 0, kv_cnt = 0;
     uint32_t s_cnt0 = 0, s_cnt1 = 0;  // S_t issued so far
@@ -239,19 +242,19 @@ __device__ void fwd_mma_s(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint
             const uint32_t n = kv_cnt + ring_pos_k(i);
             const uint32_t st = n % C::kSlots;
             if (!wd.wait(&bars->kv_full[st], (n / C::kSlots) & 1)) return;
-            const uint32_t kb = kv_base + st * C::kKvTile;
+            const uint32_t k_lo = kv_lo + st * (C::kKvTile >> 4);
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 if (!tile_uses(it, t, j)) continue;
                 uint32_t& sc = t ? s_cnt1 : s_cnt0;
                 if (sc > 0 && !wd.wait(&bars->s_free[t], (sc - 1) & 1)) return;
                 tc_fence_after();
-                const uint32_t qa = q_base + t * C::kQTile;
+                const uint32_t a_lo = q_lo + t * (C::kQTile >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::kAtomBytes + (kk & 3) * 32;
-                    umma_ss(tmem + C::col_s(t), sdesc_sw128(qa + off, 16, 1024),
-                            sdesc_sw128(kb + off, 16, 1024), kIdesc, kk > 0);
+                    const uint32_t off = ((kk >> 2) * C::kAtomBytes + (kk & 3) * 32) >> 4;
+                    umma_ss_lh(tmem + C::col_s(t), a_lo + off, d_hi, k_lo + off, d_hi, kIdesc,
+                               kk > 0);
                 }
                 umma_commit(&bars->s_full[t]);
                 ++sc;
@@ -271,8 +274,11 @@ __device__ void fwd_mma_pv(const FwdParams& p, uint8_t* smem, FwdBars* bars, uin
                            const Watchdog& wd, int n_items) {
     using C = FwdCfg<D>;
     constexpr uint32_t kIdesc = idesc_bf16_f32(128, D, false, true);
-    const uint32_t p_base = smem_u32(smem + C::kOffP);
-    const uint32_t kv_base = smem_u32(smem + C::kOffKV);
+    // A = P_t (K-major), B = V (MN-major: 64-wide d atoms kAtomBytes apart), as halves
+    const uint64_t dp = sdesc_sw128(smem_u32(smem + C::kOffP), 16, 1024);
+    const uint64_t dv = sdesc_sw128(smem_u32(smem + C::kOffKV), C::kAtomBytes, 1024);
+    const uint32_t p_lo = static_cast<uint32_t>(dp), p_hi = static_cast<uint32_t>(dp >> 32);
+    const uint32_t v_lo = static_cast<uint32_t>(dv), v_hi = static_cast<uint32_t>(dv >> 32);
     const int G = gridDim.x, cta = blockIdx.x;
     uint32_t kv_cnt = 0;
     uint32_t pv_cnt0 = 0, pv_cnt1 = 0;    // PV_t issued so far (== P_t consumed)
@@ -289,7 +295,7 @@ __device__ void fwd_mma_pv(const FwdParams& p, uint8_t* smem, FwdBars* bars, uin
             const uint32_t n = kv_cnt + ring_pos_v(i, m);
             const uint32_t st = n % C::kSlots;
             if (!wd.wait(&bars->kv_full[st], (n / C::kSlots) & 1)) return;
-            const uint32_t vb = kv_base + st * C::kKvTile;
+            const uint32_t b_lo = v_lo + st * (C::kKvTile >> 4);
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 if (!tile_uses(it, t, j)) continue;
@@ -299,13 +305,12 @@ __device__ void fwd_mma_pv(const FwdParams& p, uint8_t* smem, FwdBars* bars, uin
                 uint32_t& pc = t ? pv_cnt1 : pv_cnt0;
                 if (!wd.wait(&bars->p_full[t], pc & 1)) return;
                 tc_fence_after();
-                const uint32_t pa = p_base + t * C::kPTile;
+                const uint32_t a_lo = p_lo + t * (C::kPTile >> 4);
 #pragma unroll
                 for (int kk = 0; kk < kFwdBlockN / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::kAtomBytes + (kk & 3) * 32;
-                    umma_ss(tmem + C::col_o(t), sdesc_sw128(pa + off, 16, 1024),
-                            sdesc_sw128(vb + kk * 16 * 128, C::kAtomBytes, 1024), kIdesc,
-                            (first && kk == 0) ? 0u : 1u);
+                    const uint32_t off = ((kk >> 2) * C::kAtomBytes + (kk & 3) * 32) >> 4;
+                    umma_ss_lh(tmem + C::col_o(t), a_lo + off, p_hi, b_lo + kk * (16 * 128 >> 4),
+                               v_hi, kIdesc, (first && kk == 0) ? 0u : 1u);
                 }
                 umma_commit(&bars->pv_done[t]);
                 ++pc;
