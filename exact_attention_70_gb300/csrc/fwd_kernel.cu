@@ -324,10 +324,18 @@ __device__ void fwd_mma_pv(const FwdParams& p, uint8_t* smem, FwdBars* bars, uin
     }
 }
 
-// ---- softmax / correction / epilogue (one warpgroup per Q tile, one thread per row) -------
+// ---- softmax / correction / epilogue (eight warps per Q tile, 16 rows per warp) ----------
+//
+// Warp k of tile t (k = 0..7) owns rows 32 (k % 4) + 16 (k / 4) + [0, 16) of the tile (a warp
+// may only address the TMEM lanes of its own quarter, 32 (warp % 4) + [0, 32)).  S is read
+// with the 16-lane shape, so thread i holds rows i/4 and i/4 + 8 of those 16, two columns of
+// every 8-column chunk: 64 values, the row max and sum are completed across the 4 threads of a
+// quad, and P goes to shared memory with stmatrix.  Four such warps share each SM
+// sub-partition, enough to overlap one warp's TMEM and shared-memory latency with another's
+// exponentials.
 
-// One Q tile's view of an item (the tile index is a run-time value: both softmax warpgroups
-// run the same instruction stream, which keeps the instruction cache shared between them).
+// One Q tile's view of an item (the tile index is a run-time value: every softmax warp runs
+// the same instruction stream, which keeps the instruction cache shared between them).
 struct TileView {
     bool rows, mma;
     int tok0, imin, imax, lo, hi;
@@ -345,51 +353,52 @@ __device__ __forceinline__ TileView tile_view(const Item& it, int t) {
     return v;
 }
 
+// Address of the 16-byte unit u (8 bf16 columns) of row r in a 128-row tile stored as
+// 128-byte-swizzled atoms of 64 columns.
+__device__ __forceinline__ uint32_t sw128_unit(uint32_t base, int r, int u) {
+    return base + (u >> 3) * (128 * 128) + r * 128 + (((u & 7) ^ (r & 7)) << 4);
+}
+
 template <int D>
 __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32_t tmem,
-                            const Watchdog& wd, int n_items, int t, int quarter, int lane) {
+                            const Watchdog& wd, int n_items, int t, int k, int lane) {
     using C = FwdCfg<D>;
     uint64_t* const s_full = &bars->s_full[t];
     uint64_t* const s_free = &bars->s_free[t];
     uint64_t* const p_full = &bars->p_full[t];
     uint64_t* const pv_done = &bars->pv_done[t];
     uint64_t* const o_free = &bars->o_free[t];
-    const int row = quarter * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_off + C::col_s(t);
-    const uint32_t tO = tmem + lane_off + C::col_o(t);
-    // This row of P_t: keys [64 a, 64 a + 64) in swizzle atom a; 16-byte unit u of the row's
-    // 128 bytes sits at unit u ^ (row % 8).
-    const uint32_t p_row = smem_u32(smem + C::kOffP + t * C::kPTile) + row * 128;
-    const uint32_t r7 = row & 7;
+    const int rbase = 32 * (k & 3) + 16 * (k >> 2);   // this warp's first row
+    const int ra = rbase + (lane >> 2);                // this thread's rows ra and ra + 8
+    const int cpair = 2 * (lane & 3);                  // its columns in each 8-column chunk
+    const uint32_t tS = tmem + (static_cast<uint32_t>(rbase) << 16) + C::col_s(t);
+    const uint32_t tO = tmem + (static_cast<uint32_t>(rbase) << 16) + C::col_o(t);
+    const uint32_t p_tile = smem_u32(smem + C::kOffP + t * C::kPTile);
+    // stmatrix: this thread addresses row (lane % 8) of matrix lane / 8, where matrix m holds
+    // rows rbase + 8 (m % 2) + [0, 8) of 8-column chunk (base chunk + m / 2)
+    const int st_row = rbase + 8 * ((lane >> 3) & 1) + (lane & 7);
+    const int st_dc = lane >> 4;
     const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = f2_make(sl2, sl2);
     const int G = gridDim.x, cta = blockIdx.x;
     const int g = p.g;
-    const int row_tok = row / g, row_head = row % g;
-    const bool row_in_tile = row < g * p.tpt;
+    const int tile_rows = g * p.tpt;
     uint32_t blk = 0;  // blocks of tile t processed so far (== S_t consumed == P_t produced)
-    for (int k = 0; k * G < n_items; ++k) {
-        const int idx = item_index(k, cta, G);
+    for (int kit = 0; kit * G < n_items; ++kit) {
+        const int idx = item_index(kit, cta, G);
         if (idx >= n_items) continue;
         const Item it = load_item(p, idx);
         const TileView tv = tile_view(it, t);
         if (!tv.rows) continue;
-        const int tok = tv.tok0 + row_tok;
-        const bool valid = row_in_tile && tok < it.Lq;
-        const int head = it.kvh * g + row_head;
-        int kmin, kmax;
-        row_key_interval(tok, it.Lq, it.Lk, p.causal, p.wl, p.wr, kmin, kmax);
-        float m_run = -INFINITY, l_run = 0.f;
-        __nv_bfloat16* orow =
-            p.out + (static_cast<size_t>(it.q0 + tok) * p.Hq + head) * D;
+        // this thread's rows ra and ra + 8; packed row r is token tok0 + r / g, head kvh g + r % g
+        float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;  // l: this thread's part
         if (tv.mma) {
             for (int j = tv.lo; j < tv.hi; ++j) {
                 if (!__all_sync(0xffffffffu, wd.wait(s_full, blk & 1))) return;
                 tc_fence_after();
-                uint32_t s[128];
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4)
-                    tmem_ld32(tS + c4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c4 * 32]));
+                uint32_t s[64];
+                tmem_ld16x256_x8(tS, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+                tmem_ld16x256_x8(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
                 tmem_wait_ld();
                 // S_t is in registers: the tensor core may overwrite it with S_t(j+1)
                 tc_fence_before();
@@ -397,123 +406,185 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
                 if (lane == 0) mbar_arrive(s_free);
                 if (kv_block_masked(j, tv.imin, tv.imax, it.Lq, it.Lk, kFwdBlockN, p.causal,
                                     p.wl, p.wr)) {
-                    const int key0 = j * kFwdBlockN;
+                    const int key0 = j * kFwdBlockN + cpair;
+                    int kmin_a, kmax_a, kmin_b, kmax_b;
+                    row_key_interval(tv.tok0 + ra / g, it.Lq, it.Lk, p.causal, p.wl, p.wr,
+                                     kmin_a, kmax_a);
+                    row_key_interval(tv.tok0 + (ra + 8) / g, it.Lq, it.Lk, p.causal, p.wl, p.wr,
+                                     kmin_b, kmax_b);
 #pragma unroll
-                    for (int c = 0; c < 128; ++c) {
-                        const int key = key0 + c;
-                        if (key < kmin || key > kmax) s[c] = __float_as_uint(-INFINITY);
+                    for (int c = 0; c < 16; ++c) {
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int key = key0 + 8 * c + e;
+                            if (key < kmin_a || key > kmax_a) s[4 * c + e] = __float_as_uint(-INFINITY);
+                            if (key < kmin_b || key > kmax_b)
+                                s[4 * c + 2 + e] = __float_as_uint(-INFINITY);
+                        }
                     }
                 }
-                // row max: eight independent chains of 3-input max, then a short tree
-                float acc[8];
+                // row maxima: this thread's 32 values of each row, then across the quad
+                float xa0 = __uint_as_float(s[0]), xa1 = __uint_as_float(s[1]);
+                float xb0 = __uint_as_float(s[2]), xb1 = __uint_as_float(s[3]);
 #pragma unroll
-                for (int a = 0; a < 8; ++a) {
-                    float m = __uint_as_float(s[a]);
-#pragma unroll
-                    for (int i = 1; i < 15; i += 2)
-                        m = fmax3(m, __uint_as_float(s[a + 8 * i]),
-                                  __uint_as_float(s[a + 8 * (i + 1)]));
-                    acc[a] = fmaxf(m, __uint_as_float(s[a + 120]));
+                for (int c = 1; c < 16; c += 2) {
+                    xa0 = fmax3(xa0, __uint_as_float(s[4 * c]), __uint_as_float(s[4 * c + 4]));
+                    xa1 = fmax3(xa1, __uint_as_float(s[4 * c + 1]), __uint_as_float(s[4 * c + 5]));
+                    xb0 = fmax3(xb0, __uint_as_float(s[4 * c + 2]), __uint_as_float(s[4 * c + 6]));
+                    xb1 = fmax3(xb1, __uint_as_float(s[4 * c + 3]), __uint_as_float(s[4 * c + 7]));
                 }
-                const float mx = fmaxf(fmax3(acc[0], acc[1], acc[2]),
-                                       fmax3(fmax3(acc[3], acc[4], acc[5]), acc[6], acc[7]));
-                const float m_blk = mx * sl2;
-                const bool need = m_blk > m_run + kRescaleThreshold;
-                const float m_new = need ? m_blk : m_run;
-                const float alpha = need ? ex2_approx(m_run - m_new) : 1.f;
-                l_run *= alpha;
-                m_run = m_new;
-                const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+                float mxa = fmaxf(xa0, xa1), mxb = fmaxf(xb0, xb1);
+                mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 1));
+                mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 1));
+                mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 2));
+                mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
+                const float mba = mxa * sl2, mbb = mxb * sl2;
+                const bool need_a = mba > m_a + kRescaleThreshold;
+                const bool need_b = mbb > m_b + kRescaleThreshold;
+                const float mna = need_a ? mba : m_a, mnb = need_b ? mbb : m_b;
+                const float alpha_a = need_a ? ex2_approx(m_a - mna) : 1.f;
+                const float alpha_b = need_b ? ex2_approx(m_b - mnb) : 1.f;
+                l_a *= alpha_a;
+                l_b *= alpha_b;
+                m_a = mna;
+                m_b = mnb;
+                const float ra_ref = (m_a == -INFINITY) ? 0.f : m_a;
+                const float rb_ref = (m_b == -INFINITY) ? 0.f : m_b;
+                const uint64_t nma = f2_make(-ra_ref, -ra_ref), nmb = f2_make(-rb_ref, -rb_ref);
                 // P = exp2(s * scale*log2e - m): paired FFMA, MUFU ex2, paired sums
-                const uint64_t sl2x2 = f2_make(sl2, sl2);
-                const uint64_t negm2 = f2_make(-mref, -mref);
-                uint64_t sum2[4] = {0, 0, 0, 0};
-                uint32_t pk[64];
+                uint64_t suma = 0, sumb = 0;
+                uint32_t pka[16], pkb[16];
 #pragma unroll
-                for (int e = 0; e < 64; ++e) {
-                    const uint64_t x2 = f2_fma(
-                        f2_make(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])),
-                        sl2x2, negm2);
-                    float x0, x1;
-                    f2_split(x2, x0, x1);
-                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                    sum2[e & 3] = f2_add(sum2[e & 3], f2_make(p0, p1));
-                    pk[e] = pack_bf16x2(p0, p1);
+                for (int c = 0; c < 16; ++c) {
+                    const uint64_t xa = f2_fma(f2_make(__uint_as_float(s[4 * c]), __uint_as_float(s[4 * c + 1])),
+                                               sl2x2, nma);
+                    const uint64_t xb = f2_fma(f2_make(__uint_as_float(s[4 * c + 2]), __uint_as_float(s[4 * c + 3])),
+                                               sl2x2, nmb);
+                    float a0, a1, b0, b1;
+                    f2_split(xa, a0, a1);
+                    f2_split(xb, b0, b1);
+                    const float pa0 = ex2_approx(a0), pa1 = ex2_approx(a1);
+                    const float pb0 = ex2_approx(b0), pb1 = ex2_approx(b1);
+                    suma = f2_add(suma, f2_make(pa0, pa1));
+                    sumb = f2_add(sumb, f2_make(pb0, pb1));
+                    pka[c] = pack_bf16x2(pa0, pa1);
+                    pkb[c] = pack_bf16x2(pb0, pb1);
                 }
-                float sum;
                 {
-                    const uint64_t t2 = f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3]));
                     float lo, hi;
-                    f2_split(t2, lo, hi);
-                    sum = lo + hi;
+                    f2_split(suma, lo, hi);
+                    l_a += lo + hi;
+                    f2_split(sumb, lo, hi);
+                    l_b += lo + hi;
                 }
-                l_run += sum;
                 // PV_t of the previous block has finished reading P_t from shared memory and
                 // accumulating into O_t.
                 if (blk > 0) {
                     if (!__all_sync(0xffffffffu, wd.wait(pv_done, (blk - 1) & 1))) return;
                     tc_fence_after();
                 }
-                if (__any_sync(0xffffffffu, need) && j > tv.lo) {
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(tO + c * 32, o);
+                if (__any_sync(0xffffffffu, need_a || need_b) && j > tv.lo) {
+#pragma unroll 1
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t o[16];
+                        tmem_ld16x256_x4(tO + 32 * cc, o);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(tO + c * 32, o);
+                        for (int c = 0; c < 4; ++c) {
+                            o[4 * c] = __float_as_uint(__uint_as_float(o[4 * c]) * alpha_a);
+                            o[4 * c + 1] = __float_as_uint(__uint_as_float(o[4 * c + 1]) * alpha_a);
+                            o[4 * c + 2] = __float_as_uint(__uint_as_float(o[4 * c + 2]) * alpha_b);
+                            o[4 * c + 3] = __float_as_uint(__uint_as_float(o[4 * c + 3]) * alpha_b);
+                        }
+                        tmem_st16x256_x4(tO + 32 * cc, o);
                     }
                     tmem_wait_st();
                     tc_fence_before();
                 }
+                // P_t rows of this warp: chunks (2 cp, 2 cp + 1) x (rows ra, ra + 8) per stmatrix
 #pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    st_shared_v4(p_row + (u >> 3) * C::kAtomBytes + ((((u & 7) ^ r7)) << 4),
-                                 pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                for (int cp = 0; cp < 8; ++cp)
+                    stmatrix_x4(sw128_unit(p_tile, st_row, 2 * cp + st_dc), pka[2 * cp], pkb[2 * cp],
+                                pka[2 * cp + 1], pkb[2 * cp + 1]);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(p_full);
                 ++blk;
             }
-            // Epilogue: O / l from TMEM, bf16, straight to global memory.
+            // Epilogue: full row sums, O / l from TMEM as bf16 staged through this warp's rows
+            // of P_t (free once the last PV_t completed), then row-contiguous global stores.
+            l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+            l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+            l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+            l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
             if (!__all_sync(0xffffffffu, wd.wait(pv_done, (blk - 1) & 1))) return;
             tc_fence_after();
-            const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+            const float inv_a = l_a > 0.f ? 1.f / l_a : 0.f;
+            const float inv_b = l_b > 0.f ? 1.f / l_b : 0.f;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int cc = 0; cc < D / 64; ++cc) {
                 uint32_t o[32];
-                tmem_ld32(tO + c * 32, o);
+                tmem_ld16x256_x8(tO + 64 * cc, o);
                 tmem_wait_ld();
-                if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l,
-                                          __uint_as_float(o[8 * v + 1]) * inv_l);
-                        w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l,
-                                          __uint_as_float(o[8 * v + 3]) * inv_l);
-                        w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l,
-                                          __uint_as_float(o[8 * v + 5]) * inv_l);
-                        w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l,
-                                          __uint_as_float(o[8 * v + 7]) * inv_l);
-                        dst[v] = w;
-                    }
+                for (int cp = 0; cp < 4; ++cp) {
+                    const int c = 2 * cp;
+                    stmatrix_x4(sw128_unit(p_tile, st_row, 8 * cc + c + st_dc),
+                                pack_bf16x2(__uint_as_float(o[4 * c]) * inv_a,
+                                            __uint_as_float(o[4 * c + 1]) * inv_a),
+                                pack_bf16x2(__uint_as_float(o[4 * c + 2]) * inv_b,
+                                            __uint_as_float(o[4 * c + 3]) * inv_b),
+                                pack_bf16x2(__uint_as_float(o[4 * c + 4]) * inv_a,
+                                            __uint_as_float(o[4 * c + 5]) * inv_a),
+                                pack_bf16x2(__uint_as_float(o[4 * c + 6]) * inv_b,
+                                            __uint_as_float(o[4 * c + 7]) * inv_b));
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_free);
-        } else if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow);
+            {
+                // two threads per row: row rbase + lane / 2, units of half (lane % 2)
+                constexpr int kUnits = D / 16;
+                const int r = rbase + (lane >> 1);
+                const int tok = tv.tok0 + r / g;
+                if (r < tile_rows && tok < it.Lq) {
+                    const int head = it.kvh * g + r % g;
+                    uint4* dst = reinterpret_cast<uint4*>(
+                        p.out + (static_cast<size_t>(it.q0 + tok) * p.Hq + head) * D);
 #pragma unroll
-            for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
+                    for (int v = 0; v < kUnits; ++v) {
+                        const int u = (lane & 1) * kUnits + v;
+                        dst[u] = ld_shared_v4(sw128_unit(p_tile, r, u));
+                    }
+                }
+            }
+            __syncwarp();  // staging reads done before this warp's next P_t stores
+        } else {
+            // no visible key at all: O = 0 (each thread of the quad writes D/4 columns)
+            const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = ra + 8 * h;
+                const int tok = tv.tok0 + r / g;
+                if (r < tile_rows && tok < it.Lq) {
+                    uint4* dst = reinterpret_cast<uint4*>(
+                        p.out + (static_cast<size_t>(it.q0 + tok) * p.Hq + it.kvh * g + r % g) * D);
+#pragma unroll
+                    for (int v = 0; v < D / 32; ++v) dst[(lane & 3) * (D / 32) + v] = z;
+                }
+            }
         }
-        if (valid) {
-            p.lse[static_cast<size_t>(head) * p.total_q + it.q0 + tok] =
-                l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+        const int tok_a = tv.tok0 + ra / g, tok_b = tv.tok0 + (ra + 8) / g;
+        const bool valid_a = ra < tile_rows && tok_a < it.Lq;
+        const bool valid_b = ra + 8 < tile_rows && tok_b < it.Lq;
+        if ((lane & 3) == 0) {
+            if (valid_a)
+                p.lse[static_cast<size_t>(it.kvh * g + ra % g) * p.total_q + it.q0 + tok_a] =
+                    l_a > 0.f ? (m_a + __log2f(l_a)) * kLn2 : -INFINITY;
+            if (valid_b)
+                p.lse[static_cast<size_t>(it.kvh * g + (ra + 8) % g) * p.total_q + it.q0 + tok_b] =
+                    l_b > 0.f ? (m_b + __log2f(l_b)) * kLn2 : -INFINITY;
         }
     }
 }
@@ -526,6 +597,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     FwdBars* bars = reinterpret_cast<FwdBars*>(smem + C::kOffBar);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kSoftmaxWarps = 16;
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
@@ -536,16 +608,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&bars->s_full[t], 1);
-            mbar_init(&bars->s_free[t], 4);
-            mbar_init(&bars->p_full[t], 4);
+            mbar_init(&bars->s_free[t], kSoftmaxWarps / 2);
+            mbar_init(&bars->p_full[t], kSoftmaxWarps / 2);
             mbar_init(&bars->pv_done[t], 1);
-            mbar_init(&bars->o_free[t], 4);
+            mbar_init(&bars->o_free[t], kSoftmaxWarps / 2);
             mbar_init(&bars->drain[t], 1);
         }
         bars->abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp == 9) tmem_alloc(&bars->tmem_base, C::kTmemCols);
+    if (warp == kSoftmaxWarps + 1) tmem_alloc(&bars->tmem_base, C::kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -553,32 +625,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     const Watchdog wd{&bars->abort_flag, p.status};
     const int n_items = p.header->n_items;
 
-    // Registers: launched at 168 per thread (384 threads); warpgroup 2 (TMA, two MMA issuers,
-    // one idle warp) drops to 80 and the two softmax warpgroups rise to 208:
-    // 128 * 80 + 256 * 208 = 63488 <= 384 * 168 = 64512.
-    if (warp >= 8) {
-        regs_decrease<80>();
-        if (warp == 8) {
+    // Registers: launched at 96 per thread (640 threads); warpgroup 4 (TMA, two MMA issuers,
+    // one idle warp) drops to 64 and the four softmax warpgroups rise to 104:
+    // 128 * 64 + 512 * 104 = 61440 = 640 * 96.
+    if (warp >= kSoftmaxWarps) {
+        regs_decrease<64>();
+        if (warp == kSoftmaxWarps) {
             if (lane == 0) fwd_producer<D>(p, smem, bars, wd, n_items);
-        } else if (warp == 9 || warp == 10) {
+        } else if (warp == kSoftmaxWarps + 1 || warp == kSoftmaxWarps + 2) {
             if (lane == 0) {
-                if (warp == 9)
+                const int w = warp - kSoftmaxWarps - 1;
+                if (w == 0)
                     fwd_mma_s<D>(p, smem, bars, tmem, wd, n_items);
                 else
                     fwd_mma_pv<D>(p, smem, bars, tmem, wd, n_items);
                 // every tcgen05 op this thread issued has finished before TMEM is released
-                umma_commit(&bars->drain[warp - 9]);
-                drain_wait(&bars->drain[warp - 9], 0);
+                umma_commit(&bars->drain[w]);
+                drain_wait(&bars->drain[w], 0);
             }
         }
     } else {
-        regs_increase<208>();
-        fwd_softmax<D>(p, smem, bars, tmem, wd, n_items, warp >> 2, warp & 3, lane);
+        regs_increase<104>();
+        fwd_softmax<D>(p, smem, bars, tmem, wd, n_items, warp >> 3, warp & 7, lane);
     }
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == kSoftmaxWarps + 1) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }

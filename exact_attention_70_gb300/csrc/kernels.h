@@ -17,7 +17,7 @@ constexpr unsigned kStatusBounds = 2u;
 
 constexpr int kFwdBlockN = 128;     // keys per KV tile
 constexpr int kFwdTilesPerItem = 2; // Q tiles (of 128 packed rows) per work item
-constexpr int kFwdThreads = 384;    // 2 softmax warpgroups + (TMA warp, MMA warp, 2 idle)
+constexpr int kFwdThreads = 640;    // 4 softmax warpgroups + (TMA warp, 2 MMA warps, 1 idle)
 constexpr int kPrepThreads = 1024;
 constexpr int kPrepBins = 1024;     // cost histogram bins of the work-list sort
 
