@@ -57,6 +57,8 @@ def load():
             lib.attn_decode_num_splits.argtypes = [i32, i32, i32, i32, i32, i32]
             lib.attn_get_device_status.restype = i32
             lib.attn_get_device_status.argtypes = [P]
+            lib.attn_selftest_wait_timeout.restype = i32
+            lib.attn_selftest_wait_timeout.argtypes = [P]
             lib.attn_status_string.restype = ctypes.c_char_p
             lib.attn_status_string.argtypes = [i32]
             lib.attn_kv_block_range.restype = i32
@@ -121,6 +123,11 @@ def attn_kv_block_masked(j, i_min, i_max, seqlen_q, seqlen_k, block_n, causal, w
 def attn_get_device_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status code."""
     return int(load().attn_get_device_status(_stream(stream)))
+
+
+def attn_selftest_wait_timeout(stream=None) -> int:
+    """Launch the bounded-wait self-test kernel (its wait runs out after 20 ms)."""
+    return int(load().attn_selftest_wait_timeout(_stream(stream)))
 
 
 def _workspace(nbytes, device, workspace):

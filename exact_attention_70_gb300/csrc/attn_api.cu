@@ -338,6 +338,15 @@ attn_status_t attn_decode_kvcache(const void* q, const void* k_cache, const void
     return ATTN_OK;
 }
 
+attn_status_t attn_selftest_wait_timeout(void* stream) {
+    DeviceState* dev = nullptr;
+    attn_status_t st = device_state(&dev);
+    if (st != ATTN_OK) return st;
+    if (launch_watchdog_selftest(dev->status, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
 attn_status_t attn_get_device_status(void* stream) {
     DeviceState* dev = nullptr;
     attn_status_t st = device_state(&dev);

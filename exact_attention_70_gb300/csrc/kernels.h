@@ -60,6 +60,10 @@ cudaError_t launch_fwd_prepare(const FwdPrepParams& p, cudaStream_t stream);
 cudaError_t launch_fwd(const FwdParams& p, int head_dim, int grid, cudaStream_t stream);
 int fwd_smem_bytes(int head_dim);
 
+// ---- failure-path self-test ------------------------------------------------------------
+
+cudaError_t launch_watchdog_selftest(unsigned* status, cudaStream_t stream);
+
 // ---- decode -------------------------------------------------------------------------------
 
 constexpr int kDecChunk = 64;       // keys per pipeline stage

@@ -86,6 +86,7 @@ struct Watchdog {
         *abort_flag = 1;
     }
 
+    template <unsigned long long kLimitNs = kWaitLimitNs>
     __device__ bool wait(uint64_t* bar, uint32_t parity) const {
         if (mbar_try(bar, parity)) return true;
         const unsigned long long t0 = global_ns();
@@ -93,7 +94,7 @@ struct Watchdog {
             if (mbar_try(bar, parity)) return true;
             if ((it & 63u) == 0) {
                 if (*abort_flag) return false;
-                if (global_ns() - t0 > kWaitLimitNs) {
+                if (global_ns() - t0 > kLimitNs) {
                     fail();
                     return false;
                 }

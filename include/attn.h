@@ -162,6 +162,16 @@ int attn_decode_num_splits(int batch, int nheads_q, int nheads_kv, int max_pages
  */
 attn_status_t attn_get_device_status(void* stream);
 
+/*
+ * Failure-path self-test.  Launches, on `stream`, one small kernel whose threads wait with the
+ * attention kernels' bounded wait (limit shortened to 20 ms) on a barrier that nothing ever
+ * completes.  The wait runs out, raises the timeout bit of the device status word and the
+ * kernel returns normally: a following attn_get_device_status() returns
+ * ATTN_ERR_DEVICE_TIMEOUT (and clears it) and the context stays usable.  Returns ATTN_OK once
+ * the kernel is launched, ATTN_ERR_CUDA if the launch fails.
+ */
+attn_status_t attn_selftest_wait_timeout(void* stream);
+
 /* Static description of a status code. */
 const char* attn_status_string(attn_status_t status);
 

@@ -104,6 +104,16 @@ def test_prefill_is_deterministic(attn):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+def test_bounded_wait_reports_timeout_and_context_survives(attn):
+    # a wait on a barrier that nothing completes runs out (20 ms limit) and is reported
+    assert attn.attn_selftest_wait_timeout() == 0
+    assert attn.attn_get_device_status() == -5
+    assert attn.attn_get_device_status() == 0  # cleared
+    # the context is still usable: a small prefill still matches the oracle
+    case = synth.prefill_case([300, 77], 4, 2, 128, True, seed=9)
+    check_fwd_full(attn, case)
+
+
 def test_prefill_bad_cu_seqlens_is_reported(attn):
     case = synth.prefill_case([100, 100], 2, 2, 64, True, seed=6)
     d = to_dev(case)
