@@ -11,20 +11,21 @@
 //   * a work item is two 128-row Q tiles of one (sequence, kv head); its rows pack
 //     tokens x the g query heads of that kv head (pack_gqa), so each K/V block is loaded once
 //     for 256 query rows;
-//   * warp 8 issues TMA loads: Q once per item, then the item's K and V blocks through one
+//   * warp 16 issues TMA loads: Q once per item, then the item's K and V blocks through one
 //     ring of shared-memory slots, in the order the tensor core consumes them
 //     (K_0, K_1, V_0, K_2, V_1, ..., V_{m-1});
-//   * warp 9 issues every S_t = Q_t K^T (fp32 into TMEM columns [128 t, 128 t + 128)) and
-//     warp 10 every O_t += P_t V (O_t in TMEM columns [256 + d t, ...)), both with operands in
+//   * warp 17 issues every S_t = Q_t K^T (fp32 into TMEM columns [128 t, 128 t + 128)) and
+//     warp 18 every O_t += P_t V (O_t in TMEM columns [256 + d t, ...)), both with operands in
 //     shared memory.  An issuing thread blocks until the tensor pipe accepts each instruction
 //     and the pipe holds little beyond the one executing, so a wait between two groups on a
 //     single issuer idles the tensor cores; with two issuers one thread's waits overlap the
 //     other thread's MMAs;
-//   * warps 0-3 (tile 0) and 4-7 (tile 1) run the online softmax, one thread per TMEM lane,
-//     i.e. one thread per query row.  They release S_t as soon as it is in registers, so
-//     S_t(j+1) is computed while they exponentiate block j, and write P_t as bf16 to shared
-//     memory in the 128-byte-swizzled K-major layout the tensor core reads as the A operand;
-//   * warps 8-11 (warpgroup 2) give registers to the softmax warpgroups through setmaxnreg;
+//   * warps 0-7 (tile 0) and 8-15 (tile 1) run the online softmax, 16 query rows per warp in
+//     the MMA accumulator-fragment layout.  They release S_t as soon as it is in registers,
+//     so S_t(j+1) is computed while they exponentiate block j, and write P_t as bf16 to
+//     shared memory, with stmatrix, in the 128-byte-swizzled K-major layout the tensor core
+//     reads as the A operand;
+//   * warps 16-19 (warpgroup 4) give registers to the softmax warpgroups through setmaxnreg;
 //   * the running max only moves the accumulator's reference when it grows by more than
 //     2^8 (the result is exact for any reference; this only bounds P <= 256), so the O
 //     rescale through TMEM is rare after the first blocks.
@@ -378,6 +379,12 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
     // rows rbase + 8 (m % 2) + [0, 8) of 8-column chunk (base chunk + m / 2)
     const int st_row = rbase + 8 * ((lane >> 3) & 1) + (lane & 7);
     const int st_dc = lane >> 4;
+    // Its row address for 8-column chunk u = 2 c + st_dc (c = 0..7) is
+    // st_addr[c % 4] + (c / 4) * atom: unit (u % 8) ^ (row % 8) of atom u / 8.
+    uint32_t st_addr[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        st_addr[c] = p_tile + st_row * 128 + ((((2 * c + st_dc) ^ lane) & 7) << 4);
     const float sl2 = p.scale_log2;
     const uint64_t sl2x2 = f2_make(sl2, sl2);
     const int G = gridDim.x, cta = blockIdx.x;
@@ -392,6 +399,16 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
         if (!tv.rows) continue;
         // this thread's rows ra and ra + 8; packed row r is token tok0 + r / g, head kvh g + r % g
         float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;  // l: this thread's part
+        // Blocks needing the element mask are a prefix and a suffix of [lo, hi) (left window
+        // edge; diagonal, right window edge, ragged end): the rest, [full_lo, full_hi), is
+        // found once per item.
+        int full_lo = tv.lo, full_hi = tv.hi;
+        while (full_lo < full_hi && kv_block_masked(full_lo, tv.imin, tv.imax, it.Lq, it.Lk,
+                                                    kFwdBlockN, p.causal, p.wl, p.wr))
+            ++full_lo;
+        while (full_hi > full_lo && kv_block_masked(full_hi - 1, tv.imin, tv.imax, it.Lq, it.Lk,
+                                                    kFwdBlockN, p.causal, p.wl, p.wr))
+            --full_hi;
         if (tv.mma) {
             for (int j = tv.lo; j < tv.hi; ++j) {
                 if (!__all_sync(0xffffffffu, wd.wait(s_full, blk & 1))) return;
@@ -404,8 +421,7 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(s_free);
-                if (kv_block_masked(j, tv.imin, tv.imax, it.Lq, it.Lk, kFwdBlockN, p.causal,
-                                    p.wl, p.wr)) {
+                if (j < full_lo || j >= full_hi) {
                     const int key0 = j * kFwdBlockN + cpair;
                     int kmin_a, kmax_a, kmin_b, kmax_b;
                     row_key_interval(tv.tok0 + ra / g, it.Lq, it.Lk, p.causal, p.wl, p.wr,
@@ -504,8 +520,8 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
                 // P_t rows of this warp: chunks (2 cp, 2 cp + 1) x (rows ra, ra + 8) per stmatrix
 #pragma unroll
                 for (int cp = 0; cp < 8; ++cp)
-                    stmatrix_x4(sw128_unit(p_tile, st_row, 2 * cp + st_dc), pka[2 * cp], pkb[2 * cp],
-                                pka[2 * cp + 1], pkb[2 * cp + 1]);
+                    stmatrix_x4(st_addr[cp & 3] + (cp >> 2) * C::kAtomBytes, pka[2 * cp],
+                                pkb[2 * cp], pka[2 * cp + 1], pkb[2 * cp + 1]);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(p_full);
@@ -529,7 +545,7 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
 #pragma unroll
                 for (int cp = 0; cp < 4; ++cp) {
                     const int c = 2 * cp;
-                    stmatrix_x4(sw128_unit(p_tile, st_row, 8 * cc + c + st_dc),
+                    stmatrix_x4(st_addr[cp] + cc * C::kAtomBytes,
                                 pack_bf16x2(__uint_as_float(o[4 * c]) * inv_a,
                                             __uint_as_float(o[4 * c + 1]) * inv_a),
                                 pack_bf16x2(__uint_as_float(o[4 * c + 2]) * inv_b,
