@@ -348,6 +348,161 @@ int oracle_decode(const void* q, const void* k_cache, const void* v_cache, int d
     return bad ? -1 : 0;
 }
 
+/* ---- chunked prefill over a paged cache, with KV append and rotary embedding ---------- */
+
+/*
+ * Round x to the nearest bf16 value, ties to even, straight from the fp64 value (no detour
+ * through fp32, which could round twice).  bf16 keeps 8 significant bits and fp32's exponent
+ * range; below 2^-126 its grid spacing is 2^-133.
+ */
+uint16_t oracle_f64_to_bf16(double x) {
+    uint32_t u;
+    float f;
+    if (isnan(x)) return 0x7FC0u;
+    if (x == 0.0) {
+        f = (float)x;  /* keeps the sign of zero */
+        memcpy(&u, &f, sizeof u);
+        return (uint16_t)(u >> 16);
+    }
+    int e;
+    (void)frexp(x, &e);                  /* |x| = m 2^e, 0.5 <= m < 1 */
+    int q = e - 8;                       /* 8 significant bits: spacing 2^(e-8) */
+    if (q < -133) q = -133;              /* bf16 subnormal spacing */
+    double r = rint(ldexp(x, -q));       /* nearest integer, ties to even */
+    r = ldexp(r, q);
+    if (fabs(r) >= 0x1.0p128) r = copysign(INFINITY, x);   /* beyond the largest finite bf16 */
+    f = (float)r;                        /* exact: r has at most 8 significant bits */
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+/*
+ * Rotary position embedding of one d-vector x at table row pos: the first rot components are
+ * rotated in rot/2 planes by the angles whose cosines and sines are the table row
+ * (cosr[i], sinr[i]); components rot.. are left as they are.  Plane i pairs (x_i, x_{i+rot/2})
+ * (rotate-half form) or (x_{2i}, x_{2i+1}) (interleaved form):
+ *   (a, b) -> (a cos - b sin, a sin + b cos).
+ */
+static void rope_row(double* x, int rot, int interleaved, const double* cosr, const double* sinr) {
+    const int half = rot / 2;
+    for (int i = 0; i < half; ++i) {
+        const int ia = interleaved ? 2 * i : i;
+        const int ib = interleaved ? 2 * i + 1 : i + half;
+        const double a = x[ia], b = x[ib];
+        x[ia] = a * cosr[i] - b * sinr[i];
+        x[ib] = a * sinr[i] + b * cosr[i];
+    }
+}
+
+/* Store fp64 row src (d elements) at element index idx of a bf16 or fp64 array. */
+static void store_row(void* base, int dtype, int64_t idx, int n, const double* src) {
+    if (dtype == ORACLE_F64) {
+        double* p = (double*)base + idx;
+        for (int e = 0; e < n; ++e) p[e] = src[e];
+    } else {
+        uint16_t* p = (uint16_t*)base + idx;
+        for (int e = 0; e < n; ++e) p[e] = oracle_f64_to_bf16(src[e]);
+    }
+}
+
+/*
+ * Chunked prefill against a paged cache ("Attention kernels ...", section 五.1 and its
+ * chunked-prefill figure; "04 · FA4 ...", sections 6.1-6.2 for block_table, cache_seqlens and
+ * the in-place append of new k, v with rotary embedding).  Sequence b has q_len_b new tokens
+ * (cu_q) after ctx_b = cache_seqlens[b] cached ones.
+ *   1. Every new token i of b sits at position ctx_b + i.  Its keys (rotated when rot_dim > 0)
+ *      and values are written into k_cache / v_cache at that position through block_table
+ *      (bf16 arrays store the value rounded to bf16).
+ *   2. Every query row is rotated the same way (and rounded to bf16 for bf16 data).
+ *   3. Query i of b attends, by the visibility rule with Lq = q_len_b and
+ *      Lk = ctx_b + q_len_b (bottom-right aligned), over the cache's keys 0 .. Lk - 1.
+ * k_cache, v_cache are updated in place.  Rows are (packed token, q head) pairs; rows_t ==
+ * NULL means every total_q * Hq row in (token, head) order.  rot_cos, rot_sin are
+ * [rot_rows, rot_dim / 2].  Returns -1 on an invalid argument, length or page index.
+ */
+int oracle_kvcache_prefill(const void* q, const void* k_new, const void* v_new, int dtype,
+                           void* k_cache, void* v_cache, const int32_t* cache_seqlens,
+                           const int32_t* block_table, int max_pages, int page_size,
+                           int num_pages, const int32_t* cu_q, int batch, int Hq, int Hkv, int d,
+                           const double* rot_cos, const double* rot_sin, int rot_dim,
+                           int rot_rows, int interleaved, double scale, int causal, int wl,
+                           int wr, const int64_t* rows_t, const int32_t* rows_h,
+                           long long nrows, double* out, double* lse) {
+    if (check_common(batch, Hq, Hkv, d) || page_size <= 0 || max_pages < 0) return -1;
+    if (rot_dim < 0 || rot_dim > d || (rot_dim & 1) || (rot_dim > 0 && (!rot_cos || !rot_sin)))
+        return -1;
+    const int g = Hq / Hkv;
+    const int64_t total_q = cu_q[batch];
+    /* lengths, positions and pages */
+    for (int b = 0; b < batch; ++b) {
+        const int64_t ql = (int64_t)cu_q[b + 1] - cu_q[b];
+        const int64_t ctx = cache_seqlens[b];
+        if (ql < 0 || ctx < 0 || ctx + ql > (int64_t)max_pages * page_size) return -1;
+        if (rot_dim > 0 && ctx + ql > rot_rows) return -1;
+        for (int64_t j = 0; j < ctx + ql; ++j) {
+            const int32_t page = block_table[(int64_t)b * max_pages + j / page_size];
+            if (page < 0 || page >= num_pages) return -1;
+        }
+    }
+    /* 1. append the new keys (rotated) and values */
+    double* buf = (double*)malloc(sizeof(double) * d);
+    for (int b = 0; b < batch; ++b) {
+        for (int64_t t = cu_q[b]; t < cu_q[b + 1]; ++t) {
+            const int64_t pos = cache_seqlens[b] + (t - cu_q[b]);
+            const int32_t page = block_table[(int64_t)b * max_pages + pos / page_size];
+            for (int kvh = 0; kvh < Hkv; ++kvh) {
+                const int64_t dst = (((int64_t)page * page_size + pos % page_size) * Hkv + kvh) * d;
+                const int64_t src = (t * Hkv + kvh) * d;
+                load_row(k_new, dtype, src, d, buf);
+                if (rot_dim > 0)
+                    rope_row(buf, rot_dim, interleaved, rot_cos + pos * (rot_dim / 2),
+                             rot_sin + pos * (rot_dim / 2));
+                store_row(k_cache, dtype, dst, d, buf);
+                load_row(v_new, dtype, src, d, buf);
+                store_row(v_cache, dtype, dst, d, buf);
+            }
+        }
+    }
+    free(buf);
+    /* 2-3. rotated queries against the updated cache */
+    const long long n = rows_t ? nrows : total_q * Hq;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 4) reduction(| : bad)
+    for (long long r = 0; r < n; ++r) {
+        const int64_t t = rows_t ? rows_t[r] : r / Hq;
+        const int h = rows_t ? rows_h[r] : (int)(r % Hq);
+        if (t < 0 || t >= total_q || h < 0 || h >= Hq) { bad |= 1; continue; }
+        const int b = find_seq(cu_q, batch, t);
+        const int64_t i = t - cu_q[b];
+        const int64_t Lq = (int64_t)cu_q[b + 1] - cu_q[b];
+        const int64_t Lk = cache_seqlens[b] + Lq;
+        const int kvh = h / g;
+        double* qrow = (double*)malloc(sizeof(double) * d);
+        double* kbuf = (double*)malloc(sizeof(double) * d);
+        int64_t* koff = (int64_t*)malloc(sizeof(int64_t) * (Lk > 0 ? Lk : 1));
+        double* s_row = (double*)malloc(sizeof(double) * (Lk > 0 ? Lk : 1));
+        double* p_row = (double*)malloc(sizeof(double) * (Lk > 0 ? Lk : 1));
+        unsigned char* vis = (unsigned char*)malloc(Lk > 0 ? Lk : 1);
+        load_row(q, dtype, (t * Hq + h) * d, d, qrow);
+        if (rot_dim > 0) {
+            const int64_t pos = cache_seqlens[b] + i;
+            rope_row(qrow, rot_dim, interleaved, rot_cos + pos * (rot_dim / 2),
+                     rot_sin + pos * (rot_dim / 2));
+            if (dtype == ORACLE_BF16)
+                for (int e = 0; e < d; ++e) qrow[e] = bf16_to_f64(oracle_f64_to_bf16(qrow[e]));
+        }
+        for (int64_t j = 0; j < Lk; ++j) {
+            const int32_t page = block_table[(int64_t)b * max_pages + j / page_size];
+            koff[j] = (((int64_t)page * page_size + j % page_size) * Hkv + kvh) * d;
+            vis[j] = (unsigned char)oracle_allowed(i, j, Lq, Lk, causal, wl, wr);
+        }
+        attention_row(qrow, k_cache, v_cache, dtype, koff, vis, Lk, d, scale, s_row, p_row, kbuf,
+                      out + r * d, lse + r, NULL);
+        free(qrow); free(kbuf); free(koff); free(s_row); free(p_row); free(vis);
+    }
+    return bad ? -1 : 0;
+}
+
 /* ---- the tiled method's traffic model (for the roofline discussion) -------------------- */
 
 /*

@@ -75,6 +75,12 @@ def _load():
             lib.oracle_tiled_traffic_bytes.argtypes = [ll, ll, ll]
             lib.oracle_num_threads.restype = i32
             lib.oracle_num_threads.argtypes = []
+            lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
+            lib.oracle_f64_to_bf16.argtypes = [dbl]
+            lib.oracle_kvcache_prefill.restype = i32
+            lib.oracle_kvcache_prefill.argtypes = [P, P, P, i32, P, P, P, P, i32, i32, i32, P,
+                                                   i32, i32, i32, i32, P, P, i32, i32, i32, dbl,
+                                                   i32, i32, i32, P, P, ll, P, P]
             _lib = lib
     return _lib
 
@@ -220,6 +226,67 @@ def decode(q, k_cache, v_cache, cache_seqlens, block_table, softmax_scale, num_s
     if rows_b is None:
         return out.reshape(batch, Hq, d), lse.reshape(batch, Hq)
     return out, lse
+
+
+def f64_to_bf16_bits(x: float) -> int:
+    """bf16 bit pattern of x rounded to nearest, ties to even (directly from fp64)."""
+    return int(_load().oracle_f64_to_bf16(float(x)))
+
+
+def kvcache_prefill(q, k_new, v_new, k_cache, v_cache, cache_seqlens, block_table,
+                    cu_seqlens_q, softmax_scale, causal=True, window_left=-1, window_right=-1,
+                    rotary_cos=None, rotary_sin=None, rotary_interleaved=False,
+                    rows_t=None, rows_h=None):
+    """Chunked prefill against a paged cache, with the new k, v appended (and rotated).
+
+    q [total_q, Hq, d]; k_new, v_new [total_q, Hkv, d]; k_cache, v_cache
+    [num_pages, page_size, Hkv, d]; cache_seqlens [batch] = cached tokens before this step;
+    block_table [batch, max_pages]; rotary_cos / rotary_sin [rows, rot_dim / 2] or None.
+    The caches are not modified: updated copies are returned.
+    Returns (out, lse, k_cache_new, v_cache_new) with out [n, d], lse [n] for the chosen
+    (token, head) rows, or out [total_q, Hq, d], lse [Hq, total_q] for all rows.
+    """
+    qa, dt = _host(q)
+    kn, _ = _host(k_new)
+    vn, _ = _host(v_new)
+    kc, _ = _host(k_cache)
+    vc, _ = _host(v_cache)
+    kc, vc = kc.copy(), vc.copy()
+    total_q, Hq, d = qa.shape
+    num_pages, page_size, Hkv, _ = kc.shape
+    sl = _i32(cache_seqlens)
+    bt = _i32(block_table)
+    cu = _i32(cu_seqlens_q)
+    batch = len(cu) - 1
+    if rotary_cos is not None:
+        rc_ = np.ascontiguousarray(np.asarray(rotary_cos, dtype=np.float64))
+        rs_ = np.ascontiguousarray(np.asarray(rotary_sin, dtype=np.float64))
+        rot_rows, rot_dim = rc_.shape[0], 2 * rc_.shape[1]
+    else:
+        rc_ = rs_ = None
+        rot_rows = rot_dim = 0
+    if rows_t is None:
+        n = total_q * Hq
+        rt = rh = None
+    else:
+        rt = np.ascontiguousarray(np.asarray(rows_t), dtype=np.int64)
+        rh = np.ascontiguousarray(np.asarray(rows_h), dtype=np.int32)
+        n = len(rt)
+    out = np.zeros((n, d), np.float64)
+    lse = np.zeros((n,), np.float64)
+    rc = _load().oracle_kvcache_prefill(
+        _ptr(qa), _ptr(kn), _ptr(vn), dt, _ptr(kc), _ptr(vc), _ptr(sl), _ptr(bt), bt.shape[1],
+        page_size, num_pages, _ptr(cu), batch, Hq, Hkv, d,
+        _ptr(rc_) if rc_ is not None else None, _ptr(rs_) if rs_ is not None else None,
+        rot_dim, rot_rows, int(rotary_interleaved), float(softmax_scale), int(causal),
+        window_left, window_right, _ptr(rt) if rt is not None else None,
+        _ptr(rh) if rh is not None else None, n, _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle_kvcache_prefill rejected its arguments")
+    if rows_t is None:
+        out = out.reshape(total_q, Hq, d)
+        lse = lse.reshape(total_q, Hq).T.copy()
+    return out, lse, kc, vc
 
 
 def tiled_traffic_bytes(N, d, Br) -> int:
