@@ -59,6 +59,12 @@ def load():
             lib.attn_get_device_status.argtypes = [P]
             lib.attn_selftest_wait_timeout.restype = i32
             lib.attn_selftest_wait_timeout.argtypes = [P]
+            lib.attn_fwd_kvcache.restype = i32
+            lib.attn_fwd_kvcache.argtypes = [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, P, P,
+                                             i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                             ctypes.c_float, i32, i32, i32, P, sz, P]
+            lib.attn_fwd_kvcache_workspace_bytes.restype = sz
+            lib.attn_fwd_kvcache_workspace_bytes.argtypes = [i32] * 7
             lib.attn_status_string.restype = ctypes.c_char_p
             lib.attn_status_string.argtypes = [i32]
             lib.attn_kv_block_range.restype = i32
@@ -175,6 +181,60 @@ def attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
                       int(window_right), _ptr(ws), nbytes, _stream(stream))
     if rc != 0:
         raise AttnError(rc, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_kvcache(q, k_new, v_new, k_cache, v_cache, cache_seqlens, block_table,
+                     cu_seqlens_q, max_seqlen_q, softmax_scale=None, causal=True,
+                     window_left=-1, window_right=-1, rotary_cos=None, rotary_sin=None,
+                     rotary_interleaved=False, out=None, lse=None, workspace=None, stream=None):
+    """Chunked prefill against a paged cache; the new k, v (rotated k) are written into it.
+
+    q [total_q, Hq, d], k_new / v_new [total_q, Hkv, d] bf16; caches
+    [num_pages, page_size, Hkv, d] bf16 (updated in place); cache_seqlens [batch],
+    block_table [batch, max_pages], cu_seqlens_q [batch + 1] int32; rotary_cos / rotary_sin
+    fp32 [rows, rotary_dim / 2] or None.  Returns (out [total_q, Hq, d], lse [Hq, total_q]).
+    """
+    lib = load()
+    _check(q, "q", torch.bfloat16, 3)
+    _check(k_new, "k_new", torch.bfloat16, 3)
+    _check(v_new, "v_new", torch.bfloat16, 3)
+    _check(k_cache, "k_cache", torch.bfloat16, 4)
+    _check(v_cache, "v_cache", torch.bfloat16, 4)
+    _check(cache_seqlens, "cache_seqlens", torch.int32, 1)
+    _check(block_table, "block_table", torch.int32, 2)
+    _check(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    total_q, Hq, d = q.shape
+    num_pages, page_size, Hkv, dk = k_cache.shape
+    if v_cache.shape != k_cache.shape or dk != d or k_new.shape != (total_q, Hkv, d) or \
+            v_new.shape != k_new.shape:
+        raise ValueError("inconsistent q / k_new / v_new / cache shapes")
+    batch = cu_seqlens_q.numel() - 1
+    if cache_seqlens.numel() != batch or block_table.shape[0] != batch:
+        raise ValueError("cache_seqlens and block_table must have one row per sequence")
+    if rotary_cos is not None:
+        _check(rotary_cos, "rotary_cos", torch.float32, 2)
+        _check(rotary_sin, "rotary_sin", torch.float32, 2)
+        rot_rows, rot_dim = rotary_cos.shape[0], 2 * rotary_cos.shape[1]
+    else:
+        rot_rows = rot_dim = 0
+    scale = d ** -0.5 if softmax_scale is None else float(softmax_scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    nbytes = int(lib.attn_fwd_kvcache_workspace_bytes(max(batch, 0), total_q, int(max_seqlen_q),
+                                                      Hq, Hkv, d, rot_dim))
+    ws = _workspace(nbytes, q.device, workspace)
+    rc = lib.attn_fwd_kvcache(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                              _ptr(cache_seqlens), _ptr(block_table), _ptr(cu_seqlens_q),
+                              _ptr(rotary_cos), _ptr(rotary_sin), rot_dim, rot_rows,
+                              int(bool(rotary_interleaved)), _ptr(out), _ptr(lse), batch, total_q,
+                              int(max_seqlen_q), Hq, Hkv, d, page_size, block_table.shape[1],
+                              num_pages, scale, int(bool(causal)), int(window_left),
+                              int(window_right), _ptr(ws), nbytes, _stream(stream))
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd_kvcache")
     return out, lse
 
 

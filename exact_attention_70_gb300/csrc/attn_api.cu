@@ -176,6 +176,7 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* out, f
                                           align_up(sizeof(int) * (batch + 1), 16));
 
     FwdPrepParams pp;
+    memset(&pp, 0, sizeof(pp));
     pp.cu_q = cu_seqlens_q;
     pp.cu_k = cu_seqlens_k;
     pp.prefix = prefix;
@@ -219,6 +220,160 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* out, f
     fp.wr = window_right;
     fp.scale_log2 = softmax_scale * kLog2eF;
 
+    if (launch_fwd_prepare(pp, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (launch_fwd(fp, head_dim, dev->num_sms, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+size_t attn_fwd_kvcache_workspace_bytes(int batch, int total_q, int max_seqlen_q, int nheads_q,
+                                        int nheads_kv, int head_dim, int rotary_dim) {
+    const size_t list = attn_fwd_workspace_bytes(batch, max_seqlen_q, nheads_q, nheads_kv);
+    if (list == 0 && batch > 0) return 0;
+    if (total_q < 0 || (head_dim != 64 && head_dim != 128)) return 0;
+    const size_t qrot =
+        rotary_dim > 0 ? static_cast<size_t>(total_q) * nheads_q * head_dim * 2 : 0;
+    return align_up(list, 256) + qrot;
+}
+
+attn_status_t attn_fwd_kvcache(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                               void* v_cache, const int32_t* cache_seqlens,
+                               const int32_t* block_table, const int32_t* cu_seqlens_q,
+                               const float* rotary_cos, const float* rotary_sin, int rotary_dim,
+                               int rotary_rows, int rotary_interleaved, void* out, float* lse,
+                               int batch, int total_q, int max_seqlen_q, int nheads_q,
+                               int nheads_kv, int head_dim, int page_size,
+                               int max_pages_per_seq, int num_pages, float softmax_scale,
+                               int causal, int window_left, int window_right, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    if (batch < 0 || total_q < 0 || max_seqlen_q < 0 || nheads_q <= 0 || nheads_kv <= 0 ||
+        window_left < -1 || window_right < -1 || !scale_ok(softmax_scale) ||
+        max_pages_per_seq <= 0 || num_pages <= 0 || page_size <= 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (nheads_q % nheads_kv != 0) return ATTN_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+    const int g = nheads_q / nheads_kv;
+    if (g > 128) return ATTN_ERR_UNSUPPORTED;
+    // pages hold whole 16-row boxes and a 128-key block is whole pages or part of one
+    if (page_size % 16 != 0 || (kFwdBlockN % page_size != 0 && page_size % kFwdBlockN != 0))
+        return ATTN_ERR_UNSUPPORTED;
+    if (rotary_dim < 0 || rotary_dim > head_dim || rotary_dim % 16 != 0) return ATTN_ERR_UNSUPPORTED;
+    if (rotary_dim > 0 && (!rotary_cos || !rotary_sin || rotary_rows <= 0 ||
+                           !aligned(rotary_cos, 4) || !aligned(rotary_sin, 4)))
+        return ATTN_ERR_INVALID_ARG;
+    if (batch == 0 || total_q == 0) return ATTN_OK;
+    if (!q || !k_new || !v_new || !k_cache || !v_cache || !cache_seqlens || !block_table ||
+        !cu_seqlens_q || !out || !lse)
+        return ATTN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+        !aligned(cache_seqlens, 4) || !aligned(block_table, 4) || !aligned(cu_seqlens_q, 4))
+        return ATTN_ERR_INVALID_ARG;
+    const long long cache_rows = static_cast<long long>(num_pages) * page_size;
+    if (static_cast<long long>(total_q) * nheads_q > (1LL << 31) - 1 ||
+        cache_rows * nheads_kv > (1LL << 31) - 1 ||
+        static_cast<long long>(max_pages_per_seq) * page_size > (1LL << 30))
+        return ATTN_ERR_UNSUPPORTED;
+    const size_t need = attn_fwd_kvcache_workspace_bytes(batch, total_q, max_seqlen_q, nheads_q,
+                                                         nheads_kv, head_dim, rotary_dim);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return ATTN_ERR_WORKSPACE;
+
+    DeviceState* dev = nullptr;
+    attn_status_t st = device_state(&dev);
+    if (st != ATTN_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    const int tpt = tokens_per_tile(g);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    FwdWorkspaceHeader* header = reinterpret_cast<FwdWorkspaceHeader*>(ws);
+    int* prefix = reinterpret_cast<int*>(ws + sizeof(FwdWorkspaceHeader));
+    int4* items = reinterpret_cast<int4*>(ws + sizeof(FwdWorkspaceHeader) +
+                                          align_up(sizeof(int) * (batch + 1), 16));
+    __nv_bfloat16* q_rot =
+        rotary_dim > 0
+            ? reinterpret_cast<__nv_bfloat16*>(
+                  ws + align_up(attn_fwd_workspace_bytes(batch, max_seqlen_q, nheads_q, nheads_kv), 256))
+            : nullptr;
+
+    // 1. append the new keys (rotated) and values; rotate the queries
+    AppendParams ap;
+    ap.q = static_cast<const __nv_bfloat16*>(q);
+    ap.k_new = static_cast<const __nv_bfloat16*>(k_new);
+    ap.v_new = static_cast<const __nv_bfloat16*>(v_new);
+    ap.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+    ap.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+    ap.q_rot = q_rot;
+    ap.cu_q = cu_seqlens_q;
+    ap.cache_seqlens = cache_seqlens;
+    ap.block_table = block_table;
+    ap.rot_cos = rotary_cos;
+    ap.rot_sin = rotary_sin;
+    ap.status = dev->status;
+    ap.batch = batch;
+    ap.total_q = total_q;
+    ap.Hq = nheads_q;
+    ap.Hkv = nheads_kv;
+    ap.d = head_dim;
+    ap.page_size = page_size;
+    ap.max_pages = max_pages_per_seq;
+    ap.num_pages = num_pages;
+    ap.rot_dim = rotary_dim;
+    ap.rot_rows = rotary_rows;
+    ap.interleaved = rotary_interleaved ? 1 : 0;
+
+    // 2. work list: sequence b has q_len_b query rows and cache_seqlens[b] + q_len_b keys
+    FwdPrepParams pp;
+    memset(&pp, 0, sizeof(pp));
+    pp.cu_q = cu_seqlens_q;
+    pp.cu_k = nullptr;
+    pp.cache_seqlens = cache_seqlens;
+    pp.max_keys = max_pages_per_seq * page_size;
+    pp.prefix = prefix;
+    pp.items = items;
+    pp.header = header;
+    pp.status = dev->status;
+    pp.batch = batch;
+    pp.total_q = total_q;
+    pp.max_seqlen_q = max_seqlen_q;
+    pp.Hkv = nheads_kv;
+    pp.tpt = tpt;
+    pp.capacity_pairs = static_cast<int>(fwd_capacity_pairs(batch, max_seqlen_q, g));
+    pp.causal = causal ? 1 : 0;
+    pp.wl = window_left;
+    pp.wr = window_right;
+
+    // 3. attention over the cache, K/V gathered through block_table
+    const int box_rows = page_size < kFwdBlockN ? page_size : kFwdBlockN;
+    FwdParams fp;
+    memset(&fp, 0, sizeof(fp));
+    if (encode_3d(&fp.tm_q, q_rot ? static_cast<const void*>(q_rot) : q, head_dim, nheads_q,
+                  total_q, g, tpt) != ATTN_OK ||
+        encode_3d(&fp.tm_k, k_cache, head_dim, nheads_kv, cache_rows, 1, box_rows) != ATTN_OK ||
+        encode_3d(&fp.tm_v, v_cache, head_dim, nheads_kv, cache_rows, 1, box_rows) != ATTN_OK)
+        return ATTN_ERR_CUDA;
+    fp.out = static_cast<__nv_bfloat16*>(out);
+    fp.lse = lse;
+    fp.cu_q = cu_seqlens_q;
+    fp.cu_k = nullptr;
+    fp.items = items;
+    fp.header = header;
+    fp.status = dev->status;
+    fp.Hq = nheads_q;
+    fp.Hkv = nheads_kv;
+    fp.g = g;
+    fp.tpt = tpt;
+    fp.total_q = total_q;
+    fp.causal = pp.causal;
+    fp.wl = window_left;
+    fp.wr = window_right;
+    fp.scale_log2 = softmax_scale * kLog2eF;
+    fp.block_table = block_table;
+    fp.cache_seqlens = cache_seqlens;
+    fp.page_size = page_size;
+    fp.max_pages = max_pages_per_seq;
+    fp.num_pages = num_pages;
+    fp.box_rows = box_rows;
+
+    if (launch_kvcache_append(ap, dev->num_sms, s) != cudaSuccess) return ATTN_ERR_CUDA;
     if (launch_fwd_prepare(pp, s) != cudaSuccess) return ATTN_ERR_CUDA;
     if (launch_fwd(fp, head_dim, dev->num_sms, s) != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;

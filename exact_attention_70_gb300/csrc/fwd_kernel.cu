@@ -81,6 +81,7 @@ struct Item {
     bool any;
 };
 
+template <bool kPaged>
 __device__ __forceinline__ Item load_item(const FwdParams& p, int idx) {
     Item it;
     const int4 w = p.items[idx];
@@ -89,8 +90,13 @@ __device__ __forceinline__ Item load_item(const FwdParams& p, int idx) {
     const int m = w.z;
     it.q0 = p.cu_q[it.b];
     it.Lq = p.cu_q[it.b + 1] - it.q0;
-    it.k0 = p.cu_k[it.b];
-    it.Lk = p.cu_k[it.b + 1] - it.k0;
+    if constexpr (kPaged) {  // the cached prefix, then this call's new tokens
+        it.k0 = 0;
+        it.Lk = p.cache_seqlens[it.b] + it.Lq;
+    } else {
+        it.k0 = p.cu_k[it.b];
+        it.Lk = p.cu_k[it.b + 1] - it.k0;
+    }
     it.jlo = 1 << 30;
     it.jhi = 0;
     it.any = false;
@@ -149,7 +155,7 @@ __device__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 // ---- TMA producer (one thread) -----------------------------------------------------------
 
-template <int D>
+template <int D, bool kPaged>
 __device__ void fwd_producer_loop(const FwdParams& p, uint8_t* smem, FwdBars* bars,
                                   const Watchdog& wd, int n_items, uint32_t& q_cnt,
                                   uint32_t& kv_cnt) {
@@ -162,7 +168,7 @@ __device__ void fwd_producer_loop(const FwdParams& p, uint8_t* smem, FwdBars* ba
     for (int k = 0; k * G < n_items; ++k) {
         const int idx = item_index(k, c, G);
         if (idx >= n_items) continue;
-        const Item it = load_item(p, idx);
+        const Item it = load_item<kPaged>(p, idx);
         if (!it.any) continue;
         if (q_cnt > 0 && !wd.wait(&bars->q_empty, (q_cnt - 1) & 1)) return;
         uint32_t qbytes = 0;
@@ -191,22 +197,45 @@ __device__ void fwd_producer_loop(const FwdParams& p, uint8_t* smem, FwdBars* ba
                 return;
             mbar_arrive_expect_tx(&bars->kv_full[st], C::kKvTile);
             const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
+            uint8_t* const slot = smem + C::kOffKV + st * C::kKvTile;
+            if constexpr (!kPaged) {
 #pragma unroll
-            for (int h = 0; h < C::kHalves; ++h)
-                tma_load_3d(smem + C::kOffKV + st * C::kKvTile + h * C::kAtomBytes, map,
-                            &bars->kv_full[st], h * 64, it.kvh,
-                            it.k0 + (it.jlo + i) * kFwdBlockN);
+                for (int h = 0; h < C::kHalves; ++h)
+                    tma_load_3d(slot + h * C::kAtomBytes, map, &bars->kv_full[st], h * 64,
+                                it.kvh, it.k0 + (it.jlo + i) * kFwdBlockN);
+            } else {
+                // Gather the block's keys page by page through block_table.  Boxes wholly past
+                // the sequence end (whose table entries need not be valid) and boxes of a bad
+                // page id are aimed past the end of the cache, so TMA fills them with zeros.
+                const int* bt = p.block_table + static_cast<size_t>(it.b) * p.max_pages;
+                const int oob_row = p.num_pages * p.page_size;
+                for (int r0 = 0; r0 < kFwdBlockN; r0 += p.box_rows) {
+                    const int key = (it.jlo + i) * kFwdBlockN + r0;
+                    int row = oob_row;
+                    if (key < it.Lk) {
+                        const int page = bt[key / p.page_size];
+                        if (page >= 0 && page < p.num_pages)
+                            row = page * p.page_size + key % p.page_size;
+                        else
+                            atomicOr(p.status, kStatusBounds);
+                    }
+#pragma unroll
+                    for (int h = 0; h < C::kHalves; ++h)
+                        tma_load_3d(slot + h * C::kAtomBytes + r0 * 128, map, &bars->kv_full[st],
+                                    h * 64, it.kvh, row);
+                }
+            }
         }
         kv_cnt += 2 * m;
     }
 }
 
-template <int D>
+template <int D, bool kPaged>
 __device__ void fwd_producer(const FwdParams& p, uint8_t* smem, FwdBars* bars,
                              const Watchdog& wd, int n_items) {
     using C = FwdCfg<D>;
     uint32_t q_cnt = 0, kv_cnt = 0;
-    fwd_producer_loop<D>(p, smem, bars, wd, n_items, q_cnt, kv_cnt);
+    fwd_producer_loop<D, kPaged>(p, smem, bars, wd, n_items, q_cnt, kv_cnt);
     // Every slot holds at most one load in flight: wait for the latest load of each one.
     if (q_cnt > 0) drain_wait(&bars->q_full, (q_cnt - 1) & 1);
     for (uint32_t st = 0; st < C::kSlots && st < kv_cnt; ++st)
@@ -217,7 +246,7 @@ __device__ void fwd_producer(const FwdParams& p, uint8_t* smem, FwdBars* bars,
 
 // S_t(j) for every (j, t) of every item.  S_t(j) overwrites the TMEM columns of S_t(j-1), so
 // it waits for tile t's softmax to have read them (s_free).
-template <int D>
+template <int D, bool kPaged>
 __device__ void fwd_mma_s(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32_t tmem,
                           const Watchdog& wd, int n_items) {
     using C = FwdCfg<D>;
@@ -233,7 +262,7 @@ __device__ void fwd_mma_s(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint
     for (int k = 0; k * G < n_items; ++k) {
         const int idx = item_index(k, cta, G);
         if (idx >= n_items) continue;
-        const Item it = load_item(p, idx);
+        const Item it = load_item<kPaged>(p, idx);
         if (!it.any) continue;
         if (!wd.wait(&bars->q_full, q_cnt & 1)) return;
         ++q_cnt;
@@ -270,7 +299,7 @@ __device__ void fwd_mma_s(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint
 // O_t (+)= P_t(j) V_j for every (j, t) of every item, P_t from shared memory.  The item's
 // first PV_t overwrites O_t, so it first waits for the previous item's epilogue to have read
 // O_t (o_free).
-template <int D>
+template <int D, bool kPaged>
 __device__ void fwd_mma_pv(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32_t tmem,
                            const Watchdog& wd, int n_items) {
     using C = FwdCfg<D>;
@@ -287,7 +316,7 @@ __device__ void fwd_mma_pv(const FwdParams& p, uint8_t* smem, FwdBars* bars, uin
     for (int k = 0; k * G < n_items; ++k) {
         const int idx = item_index(k, cta, G);
         if (idx >= n_items) continue;
-        const Item it = load_item(p, idx);
+        const Item it = load_item<kPaged>(p, idx);
         if (!it.any) continue;
         bool first0 = true, first1 = true;
         const int m = it.jhi - it.jlo;
@@ -360,7 +389,7 @@ __device__ __forceinline__ uint32_t sw128_unit(uint32_t base, int r, int u) {
     return base + (u >> 3) * (128 * 128) + r * 128 + (((u & 7) ^ (r & 7)) << 4);
 }
 
-template <int D>
+template <int D, bool kPaged>
 __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32_t tmem,
                             const Watchdog& wd, int n_items, int t, int k, int lane) {
     using C = FwdCfg<D>;
@@ -391,10 +420,13 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
     const int g = p.g;
     const int tile_rows = g * p.tpt;
     uint32_t blk = 0;  // blocks of tile t processed so far (== S_t consumed == P_t produced)
+    uint32_t kv_cnt = 0;  // K/V ring slots filled for earlier items (locates paged V blocks)
     for (int kit = 0; kit * G < n_items; ++kit) {
         const int idx = item_index(kit, cta, G);
         if (idx >= n_items) continue;
-        const Item it = load_item(p, idx);
+        const Item it = load_item<kPaged>(p, idx);
+        const uint32_t kv_base = kv_cnt;
+        if (it.any) kv_cnt += 2 * (it.jhi - it.jlo);
         const TileView tv = tile_view(it, t);
         if (!tv.rows) continue;
         // this thread's rows ra and ra + 8; packed row r is token tok0 + r / g, head kvh g + r % g
@@ -492,6 +524,25 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
                     l_a += lo + hi;
                     f2_split(sumb, lo, hi);
                     l_b += lo + hi;
+                }
+                // Paged K/V: the last block's rows past the sequence end come from cache slots
+                // nobody wrote; their P is 0 but 0 * NaN would still poison O, so this tile's
+                // warps clear those V rows (whole rows: the swizzle only permutes within a row).
+                if (kPaged && (j + 1) * kFwdBlockN > it.Lk) {
+                    const int m = it.jhi - it.jlo;
+                    const uint32_t n = kv_base + ring_pos_v(j - it.jlo, m);
+                    const uint32_t st = n % C::kSlots;
+                    if (!__all_sync(0xffffffffu, wd.wait(&bars->kv_full[st], (n / C::kSlots) & 1)))
+                        return;
+                    const int valid = it.Lk - j * kFwdBlockN;
+                    const uint32_t vslot = smem_u32(smem + C::kOffKV + st * C::kKvTile);
+                    const int units = (kFwdBlockN - valid) * C::kHalves * 8;
+                    for (int u = k * 32 + lane; u < units; u += 8 * 32) {
+                        const int r = valid + u / (C::kHalves * 8);
+                        const int hc = u % (C::kHalves * 8);
+                        st_shared_v4(vslot + (hc >> 3) * C::kAtomBytes + r * 128 + (hc & 7) * 16,
+                                     0u, 0u, 0u, 0u);
+                    }
                 }
                 // PV_t of the previous block has finished reading P_t from shared memory and
                 // accumulating into O_t.
@@ -605,7 +656,7 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
     }
 }
 
-template <int D>
+template <int D, bool kPaged>
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdParams p) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -647,14 +698,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     if (warp >= kSoftmaxWarps) {
         regs_decrease<64>();
         if (warp == kSoftmaxWarps) {
-            if (lane == 0) fwd_producer<D>(p, smem, bars, wd, n_items);
+            if (lane == 0) fwd_producer<D, kPaged>(p, smem, bars, wd, n_items);
         } else if (warp == kSoftmaxWarps + 1 || warp == kSoftmaxWarps + 2) {
             if (lane == 0) {
                 const int w = warp - kSoftmaxWarps - 1;
                 if (w == 0)
-                    fwd_mma_s<D>(p, smem, bars, tmem, wd, n_items);
+                    fwd_mma_s<D, kPaged>(p, smem, bars, tmem, wd, n_items);
                 else
-                    fwd_mma_pv<D>(p, smem, bars, tmem, wd, n_items);
+                    fwd_mma_pv<D, kPaged>(p, smem, bars, tmem, wd, n_items);
                 // every tcgen05 op this thread issued has finished before TMEM is released
                 umma_commit(&bars->drain[w]);
                 drain_wait(&bars->drain[w], 0);
@@ -662,7 +713,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         }
     } else {
         regs_increase<104>();
-        fwd_softmax<D>(p, smem, bars, tmem, wd, n_items, warp >> 3, warp & 7, lane);
+        fwd_softmax<D, kPaged>(p, smem, bars, tmem, wd, n_items, warp >> 3, warp & 7, lane);
     }
     __syncwarp();
     tc_fence_before();
@@ -702,6 +753,12 @@ __device__ int block_exclusive_scan(int v, int* warp_tot, int& total) {
     return before;
 }
 
+// Keys of sequence b: the contiguous K/V's range, or the cached prefix plus the new tokens.
+__device__ __forceinline__ int seq_keys(const FwdPrepParams& p, int b) {
+    return p.cache_seqlens != nullptr ? p.cache_seqlens[b] + (p.cu_q[b + 1] - p.cu_q[b])
+                                      : p.cu_k[b + 1] - p.cu_k[b];
+}
+
 __device__ int item_cost(const FwdPrepParams& p, int Lq, int Lk, int m) {
     int cost = 0;
     for (int t = 0; t < 2; ++t) {
@@ -723,10 +780,15 @@ __global__ void __launch_bounds__(kPrepThreads) fwd_prepare_kernel(FwdPrepParams
     __syncthreads();
     // 1. the sequence boundaries must describe rows inside the tensors
     for (int b = tid; b < p.batch; b += blockDim.x) {
-        const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1], k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
-        if (q0 < 0 || q1 < q0 || q1 > p.total_q || q1 - q0 > p.max_seqlen_q || k0 < 0 ||
-            k1 < k0 || k1 > p.total_k || k1 - k0 > p.max_seqlen_k)
-            err = 1;
+        const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
+        if (q0 < 0 || q1 < q0 || q1 > p.total_q || q1 - q0 > p.max_seqlen_q) err = 1;
+        if (p.cache_seqlens != nullptr) {
+            const int ctx = p.cache_seqlens[b];
+            if (ctx < 0 || static_cast<long long>(ctx) + (q1 - q0) > p.max_keys) err = 1;
+        } else {
+            const int k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
+            if (k0 < 0 || k1 < k0 || k1 > p.total_k || k1 - k0 > p.max_seqlen_k) err = 1;
+        }
     }
     __syncthreads();
     if (err) {
@@ -771,7 +833,7 @@ __global__ void __launch_bounds__(kPrepThreads) fwd_prepare_kernel(FwdPrepParams
             if (p.prefix[mid] <= q) lo = mid; else hi = mid - 1;
         }
         const int b = lo, m = q - p.prefix[b];
-        const int cost = item_cost(p, p.cu_q[b + 1] - p.cu_q[b], p.cu_k[b + 1] - p.cu_k[b], m);
+        const int cost = item_cost(p, p.cu_q[b + 1] - p.cu_q[b], seq_keys(p, b), m);
         atomicAdd(&hist[kPrepBins - 1 - min(cost, kPrepBins - 1)], 1);
     }
     __syncthreads();
@@ -786,7 +848,7 @@ __global__ void __launch_bounds__(kPrepThreads) fwd_prepare_kernel(FwdPrepParams
             if (p.prefix[mid] <= q) lo = mid; else hi = mid - 1;
         }
         const int b = lo, m = q - p.prefix[b];
-        const int cost = item_cost(p, p.cu_q[b + 1] - p.cu_q[b], p.cu_k[b + 1] - p.cu_k[b], m);
+        const int cost = item_cost(p, p.cu_q[b + 1] - p.cu_q[b], seq_keys(p, b), m);
         const int slot = atomicAdd(&hist[kPrepBins - 1 - min(cost, kPrepBins - 1)], 1);
         for (int h = 0; h < p.Hkv; ++h)
             p.items[static_cast<size_t>(slot) * p.Hkv + h] = make_int4(b, h, m, cost);
@@ -804,11 +866,12 @@ int fwd_smem_bytes(int head_dim) {
 }
 
 cudaError_t configure_fwd_kernels() {
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         FwdCfg<128>::kSmem);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                FwdCfg<64>::kSmem);
+    const cudaFuncAttribute smem = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<128, false>, smem, FwdCfg<128>::kSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(fwd_kernel<64, false>, smem, FwdCfg<64>::kSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(fwd_kernel<128, true>, smem, FwdCfg<128>::kSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(fwd_kernel<64, true>, smem, FwdCfg<64>::kSmem);
+    return e;
 }
 
 cudaError_t launch_fwd_prepare(const FwdPrepParams& p, cudaStream_t stream) {
@@ -816,11 +879,20 @@ cudaError_t launch_fwd_prepare(const FwdPrepParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// K/V through block_table when p.block_table is set, else contiguous.
 cudaError_t launch_fwd(const FwdParams& p, int head_dim, int grid, cudaStream_t stream) {
-    if (head_dim == 128)
-        fwd_kernel<128><<<grid, kFwdThreads, FwdCfg<128>::kSmem, stream>>>(p);
-    else
-        fwd_kernel<64><<<grid, kFwdThreads, FwdCfg<64>::kSmem, stream>>>(p);
+    const bool paged = p.block_table != nullptr;
+    if (head_dim == 128) {
+        if (paged)
+            fwd_kernel<128, true><<<grid, kFwdThreads, FwdCfg<128>::kSmem, stream>>>(p);
+        else
+            fwd_kernel<128, false><<<grid, kFwdThreads, FwdCfg<128>::kSmem, stream>>>(p);
+    } else {
+        if (paged)
+            fwd_kernel<64, true><<<grid, kFwdThreads, FwdCfg<64>::kSmem, stream>>>(p);
+        else
+            fwd_kernel<64, false><<<grid, kFwdThreads, FwdCfg<64>::kSmem, stream>>>(p);
+    }
     return cudaGetLastError();
 }
 

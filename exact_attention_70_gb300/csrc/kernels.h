@@ -30,7 +30,9 @@ struct FwdWorkspaceHeader {
 
 struct FwdPrepParams {
     const int* cu_q;
-    const int* cu_k;
+    const int* cu_k;            // contiguous K/V: key offsets [batch + 1]; null when paged
+    const int* cache_seqlens;   // paged K/V: cached tokens per sequence before the new ones
+    int max_keys;               // paged K/V: max_pages_per_seq * page_size
     int* prefix;     // [batch + 1] work items per sequence, exclusive scan
     int4* items;     // [capacity_pairs * Hkv]
     FwdWorkspaceHeader* header;
@@ -47,14 +49,40 @@ struct FwdParams {
     __nv_bfloat16* out;
     float* lse;
     const int* cu_q;
-    const int* cu_k;
+    const int* cu_k;            // contiguous K/V; null when paged
     const int4* items;
     const FwdWorkspaceHeader* header;
     unsigned* status;
     int Hq, Hkv, g, tpt, total_q;
     int causal, wl, wr;
     float scale_log2;  // softmax_scale * log2(e)
+    // Paged K/V (block_table != null): tm_k / tm_v are 3-D over [num_pages * page_size, Hkv, d]
+    // with boxes {64, 1, box_rows}; sequence b holds cache_seqlens[b] + q_len_b keys.
+    const int* block_table;     // [batch, max_pages]
+    const int* cache_seqlens;
+    int page_size, max_pages, num_pages, box_rows;
 };
+
+// ---- paged-cache append (chunked prefill) ---------------------------------------------------
+
+struct AppendParams {
+    const __nv_bfloat16* q;      // [total_q, Hq, d]
+    const __nv_bfloat16* k_new;  // [total_q, Hkv, d]
+    const __nv_bfloat16* v_new;
+    __nv_bfloat16* k_cache;      // [num_pages, page_size, Hkv, d]
+    __nv_bfloat16* v_cache;
+    __nv_bfloat16* q_rot;        // [total_q, Hq, d] rotated queries (rotary only)
+    const int* cu_q;
+    const int* cache_seqlens;
+    const int* block_table;
+    const float* rot_cos;        // [rot_rows, rot_dim / 2]
+    const float* rot_sin;
+    unsigned* status;
+    int batch, total_q, Hq, Hkv, d, page_size, max_pages, num_pages;
+    int rot_dim, rot_rows, interleaved;
+};
+
+cudaError_t launch_kvcache_append(const AppendParams& p, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_fwd_prepare(const FwdPrepParams& p, cudaStream_t stream);
 cudaError_t launch_fwd(const FwdParams& p, int head_dim, int grid, cudaStream_t stream);

@@ -131,6 +131,76 @@ def decode_case(lengths, Hq, Hkv, d, page_size, seed, max_pages=None, num_splits
     )
 
 
+@dataclass
+class KvcacheCase:
+    """Chunked prefill against a paged cache (new tokens appended in the same call)."""
+    name: str
+    q: torch.Tensor            # [total_q, Hq, d] bf16
+    k_new: torch.Tensor        # [total_q, Hkv, d] bf16
+    v_new: torch.Tensor
+    k_cache: torch.Tensor      # [num_pages, page_size, Hkv, d] bf16 (prefix + unused slots)
+    v_cache: torch.Tensor
+    cache_seqlens: torch.Tensor  # [batch] int32, cached tokens before the call
+    block_table: torch.Tensor    # [batch, max_pages] int32
+    cu_seqlens_q: torch.Tensor   # [batch + 1] int32
+    max_seqlen_q: int
+    page_size: int
+    softmax_scale: float
+    causal: bool
+    window_left: int
+    window_right: int
+    rotary_cos: torch.Tensor = None   # [rows, rot / 2] fp32
+    rotary_sin: torch.Tensor = None
+    rotary_interleaved: bool = False
+
+
+def rotary_tables(rows, rot_dim, base=10000.0):
+    """Standard rotary tables: row p, plane i holds the angle p * base^(-2i / rot_dim)."""
+    inv = base ** (-torch.arange(0, rot_dim, 2, dtype=torch.float64) / rot_dim)
+    ang = torch.arange(rows, dtype=torch.float64)[:, None] * inv[None, :]
+    return torch.cos(ang).float(), torch.sin(ang).float()
+
+
+def kvcache_case(q_lens, ctx_lens, Hq, Hkv, d, page_size, seed, rotary_dim=0,
+                 rotary_interleaved=False, causal=True, window=(-1, -1), spare_pages=2,
+                 poison_unused=False, scale=None, name="kvcache") -> KvcacheCase:
+    """Pages for ctx + q_len tokens per sequence, in a seeded random order; the cache's other
+    slots hold random values (or NaN with poison_unused, which must never reach a result)."""
+    g = torch.Generator().manual_seed(seed)
+    lens = [int(c) + int(n) for c, n in zip(ctx_lens, q_lens)]
+    pages_per = [max(1, (L + page_size - 1) // page_size) for L in lens]
+    num_pages = sum(pages_per) + spare_pages
+    max_pages = max(pages_per)
+    perm = torch.randperm(num_pages, generator=g).to(torch.int32)
+    bt = torch.zeros((len(lens), max_pages), dtype=torch.int32)
+    off = 0
+    for b, n in enumerate(pages_per):
+        bt[b, :n] = perm[off:off + n]
+        off += n
+    total_q = sum(int(n) for n in q_lens)
+    k_cache = randn_bf16((num_pages, page_size, Hkv, d), seed, 4)
+    v_cache = randn_bf16((num_pages, page_size, Hkv, d), seed, 5)
+    if poison_unused:
+        keep = torch.zeros((num_pages, page_size), dtype=torch.bool)
+        for b, c in enumerate(ctx_lens):
+            for j in range(int(c)):
+                keep[bt[b, j // page_size], j % page_size] = True
+        k_cache[~keep] = float("nan")
+        v_cache[~keep] = float("nan")
+    cos = sin = None
+    if rotary_dim:
+        cos, sin = rotary_tables(max(lens) + 1, rotary_dim)
+    return KvcacheCase(
+        name=name, q=randn_bf16((total_q, Hq, d), seed, 1),
+        k_new=randn_bf16((total_q, Hkv, d), seed, 2), v_new=randn_bf16((total_q, Hkv, d), seed, 3),
+        k_cache=k_cache, v_cache=v_cache,
+        cache_seqlens=torch.tensor([int(c) for c in ctx_lens], dtype=torch.int32),
+        block_table=bt, cu_seqlens_q=cu_from_lengths(q_lens), max_seqlen_q=max(int(n) for n in q_lens),
+        page_size=page_size, softmax_scale=d ** -0.5 if scale is None else scale,
+        causal=causal, window_left=window[0], window_right=window[1],
+        rotary_cos=cos, rotary_sin=sin, rotary_interleaved=rotary_interleaved)
+
+
 # ---- the five workload configurations ------------------------------------------------
 
 CONFIG_NAMES = {

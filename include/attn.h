@@ -147,6 +147,54 @@ attn_status_t attn_decode_kvcache_noalloc(const void* q, const void* k_cache,
                                           int max_pages_per_seq, int num_pages,
                                           float softmax_scale, void* stream);
 
+/*
+ * Chunked prefill against a paged KV cache, with the new keys and values appended in place
+ * ("Attention kernels: FlashAttention and PagedAttention", section 五.1 and its chunked-prefill
+ * figure; "04 · FA4 (CuTeDSL) and engineering interfaces", sections 6.1-6.2).
+ *
+ * Sequence b has q_len_b = cu_seqlens_q[b+1] - cu_seqlens_q[b] new tokens after
+ * cache_seqlens[b] cached ones.  The call
+ *   1. writes each new token's key (rotated, when rotary_dim > 0) and value into k_cache /
+ *      v_cache at position cache_seqlens[b] + i through block_table;
+ *   2. rotates the queries the same way (into the workspace; q itself is not modified);
+ *   3. computes, for every query row, exact attention over the cache's keys
+ *      0 .. cache_seqlens[b] + q_len_b - 1 with the bottom-right causal / window rule
+ *      (query i sits at key position cache_seqlens[b] + i).
+ * cache_seqlens is not advanced: the caller adds q_len_b after the call.
+ *
+ *   q            bf16 [total_q, nheads_q, head_dim]
+ *   k_new, v_new bf16 [total_q, nheads_kv, head_dim]
+ *   k_cache, v_cache  bf16 [num_pages, page_size, nheads_kv, head_dim], updated in place
+ *   cache_seqlens int32 [batch], block_table int32 [batch, max_pages_per_seq] (device);
+ *                entries past ceil((cache_seqlens[b] + q_len_b) / page_size) are not read
+ *   cu_seqlens_q int32 [batch + 1] (device)
+ *   rotary_cos, rotary_sin  fp32 [rotary_rows, rotary_dim / 2] (device), row = position;
+ *                NULL with rotary_dim = 0 for no rotary embedding.  Planes pair
+ *                (x_i, x_{i + rotary_dim/2}) or, with rotary_interleaved, (x_2i, x_2i+1):
+ *                (a, b) -> (a cos - b sin, a sin + b cos), computed in fp32, stored as bf16.
+ *   out bf16 [total_q, nheads_q, head_dim]; lse fp32 [nheads_q, total_q] (natural log)
+ *   head_dim 64 or 128; page_size a multiple of 16 that divides 128 or is a multiple of 128;
+ *   rotary_dim a multiple of 16 (0 = none); softmax_scale > 0; windows -1 = unbounded.
+ *   workspace: attn_fwd_kvcache_workspace_bytes(...) bytes, 256-byte aligned.
+ * Ownership: caller's buffers; nothing is allocated.  Errors: argument checks before any
+ * launch; an out-of-range page id, position or rotary row raises ATTN_ERR_DEVICE_BOUNDS
+ * (read with attn_get_device_status) and that row is skipped.
+ */
+attn_status_t attn_fwd_kvcache(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                               void* v_cache, const int32_t* cache_seqlens,
+                               const int32_t* block_table, const int32_t* cu_seqlens_q,
+                               const float* rotary_cos, const float* rotary_sin, int rotary_dim,
+                               int rotary_rows, int rotary_interleaved, void* out, float* lse,
+                               int batch, int total_q, int max_seqlen_q, int nheads_q,
+                               int nheads_kv, int head_dim, int page_size,
+                               int max_pages_per_seq, int num_pages, float softmax_scale,
+                               int causal, int window_left, int window_right, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* Workspace bytes for attn_fwd_kvcache (the work list plus, with rotary, the rotated q). */
+size_t attn_fwd_kvcache_workspace_bytes(int batch, int total_q, int max_seqlen_q, int nheads_q,
+                                        int nheads_kv, int head_dim, int rotary_dim);
+
 /* Bytes of split-partial workspace for attn_decode_kvcache; num_splits 0 sizes for the
  * automatic choice (at most 16 splits).  0 when one split needs no workspace. */
 size_t attn_decode_workspace_bytes(int batch, int nheads_q, int head_dim, int num_splits);

@@ -153,3 +153,34 @@ def test_block_figure_from_the_library(golden):
                     row += "D" if kb == qb else "E"
             rows.append(row)
         assert rows == ex[key]
+
+
+def test_kvcache_arguments_are_rejected_before_any_launch(lib):
+    P = ctypes.c_void_p
+    fake = P(4096)
+    f = lib.attn_fwd_kvcache
+    args = dict(q=fake, kn=fake, vn=fake, kc=fake, vc=fake, sl=fake, bt=fake, cuq=fake,
+                cos=None, sin=None, rot=0, rows=0, inter=0, out=fake, lse=fake, batch=2, tq=16,
+                mq=8, hq=8, hkv=2, d=128, ps=64, mp=4, np_=16, scale=0.1, causal=1, wl=-1, wr=-1,
+                ws=fake, wsb=1 << 22, stream=None)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return f(*a.values())
+
+    assert call(ps=48) == -2                  # page neither divides 128 nor is a multiple
+    assert call(ps=8) == -2                   # not a multiple of 16
+    assert call(ps=192) == -2                 # multiple of 64 but not of 128
+    assert call(rot=24, cos=fake, sin=fake, rows=10) == -2   # rotary_dim not a multiple of 16
+    assert call(rot=64) == -1                 # rotary without tables
+    assert call(d=96) == -2
+    assert call(hq=6, hkv=4) == -1
+    assert call(kn=None) == -1
+    assert call(q=P(4098)) == -1              # misaligned
+    assert call(ws=None) == -3
+    assert call(batch=0) == 0
+    # workspace: the work list, plus the rotated q with rotary
+    base = binding.attn_fwd_workspace_bytes(2, 8, 8, 2)
+    assert lib.attn_fwd_kvcache_workspace_bytes(2, 16, 8, 8, 2, 128, 0) == (base + 255) // 256 * 256
+    assert lib.attn_fwd_kvcache_workspace_bytes(2, 16, 8, 8, 2, 128, 64) == \
+        (base + 255) // 256 * 256 + 16 * 8 * 128 * 2
