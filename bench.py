@@ -362,6 +362,36 @@ def run_ours(args, rank, world, local):
             extra[f"cfg{cfg}"] = {"workload": synth.CONFIG_NAMES[cfg], "ms": round(ms, 4),
                                   "tflops": round(fl / ms / 1e9, 2)}
             del cq, ck, cv, co
+        # chunked prefill against the paged cache (append + rotary + attention, one call)
+        c = synth.chunked_case()
+        t = {f: getattr(c, f) for f in ("q", "k_new", "v_new", "k_cache", "v_cache",
+                                        "cache_seqlens", "block_table", "cu_seqlens_q",
+                                        "rotary_cos", "rotary_sin")}
+        t = {f: x.to(dev) for f, x in t.items()}
+        co = torch.empty_like(t["q"])
+        cl = torch.empty((t["q"].shape[1], t["q"].shape[0]), dtype=torch.float32, device=dev)
+
+        def run_k():
+            binding.attn_fwd_kvcache(t["q"], t["k_new"], t["v_new"], t["k_cache"], t["v_cache"],
+                                     t["cache_seqlens"], t["block_table"], t["cu_seqlens_q"],
+                                     c.max_seqlen_q, c.softmax_scale, c.causal, -1, -1,
+                                     t["rotary_cos"], t["rotary_sin"], False, out=co, lse=cl)
+        for _ in range(5):
+            run_k()
+        reps = 20
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            run_k()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        ql = (c.cu_seqlens_q[1:] - c.cu_seqlens_q[:-1]).tolist()
+        lk = [int(x) + n for x, n in zip(c.cache_seqlens.tolist(), ql)]
+        fl = workload.prefill_flops(ql, lk, t["q"].shape[1], t["q"].shape[2], True)
+        extra["chunked"] = {"workload": synth.CHUNKED_NAME, "ms": round(ms, 4),
+                            "tflops": round(fl / ms / 1e9, 2)}
+        del t, co
     return dict(p_flops=p_flops, d_bytes=d_bytes, total_ms=total_ms, pre_ms=pre_ms,
                 dec_ms=dec_ms, e2e_pre=e2e_pre, e2e_dec=e2e_dec, h2d_pre=h2d_pre,
                 d2h_pre=d2h_pre, h2d_dec=h2d_dec, d2h_dec=d2h_dec, clocks=clk, splits=splits,

@@ -232,3 +232,14 @@ def config_case(cfg: int):
         raise ValueError(cfg)
     c.meta["config"] = CONFIG_NAMES[cfg]
     return c
+
+
+CHUNKED_NAME = ("chunked prefill over a paged cache: 8 seqs, ctx~U[2048,16384] cached + 2048 new "
+                "tokens each, Hq=32 Hkv=8 d=128 page=256 rotary=128, causal")
+
+
+def chunked_case() -> KvcacheCase:
+    g = torch.Generator().manual_seed(1100)
+    ctx = torch.randint(2048, 16384 + 1, (8,), generator=g).tolist()
+    return kvcache_case([2048] * 8, ctx, 32, 8, 128, 256, seed=1101, rotary_dim=128,
+                        name="chunked")
