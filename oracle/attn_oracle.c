@@ -348,6 +348,99 @@ int oracle_decode(const void* q, const void* k_cache, const void* v_cache, int d
     return bad ? -1 : 0;
 }
 
+/* ---- backward pass ---------------------------------------------------------------------- */
+
+/*
+ * Gradients of L = sum(O * dO) for the standard attention of oracle_attn_fwd ("Attention
+ * kernels ...", section 四.3: the backward recomputes S = Q K^T and P = exp(S - LSE), and with
+ * D_i = rowsum(dO_i * O_i) forms dV = P^T dO, dP = dO V^T, dS = P * (dP - D), dQ = scale dS K,
+ * dK = scale dS^T Q).  Written out per query row from the definition: the row's S, P and dP
+ * are materialised, D_i = sum_j P_ij dP_ij (which equals dO_i . O_i), and the row's
+ * contributions go to dQ_i, dK_j, dV_j.  A kv head's dK, dV sum the contributions of its g
+ * query heads.  Parallel over (sequence, kv head), so no two threads touch one dK or dV row.
+ * dq [total_q, Hq, d], dk / dv [total_k, Hkv, d], dsum (D) [Hq, total_q]; all fp64.
+ */
+int oracle_attn_bwd(const void* q, const void* k, const void* v, const void* dout, int dtype,
+                    const int32_t* cu_q, const int32_t* cu_k, int batch, int Hq, int Hkv, int d,
+                    double scale, int causal, int wl, int wr, double* dq, double* dk, double* dv,
+                    double* dsum) {
+    if (check_common(batch, Hq, Hkv, d)) return -1;
+    const int g = Hq / Hkv;
+    const int64_t total_q = cu_q[batch], total_k = cu_k[batch];
+    for (int64_t i = 0; i < total_q * Hq * d; ++i) dq[i] = 0.0;
+    for (int64_t i = 0; i < total_k * Hkv * d; ++i) { dk[i] = 0.0; dv[i] = 0.0; }
+    int bad = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1) reduction(| : bad)
+    for (int b = 0; b < batch; ++b) {
+        for (int kvh = 0; kvh < Hkv; ++kvh) {
+            const int64_t q0 = cu_q[b], k0 = cu_k[b];
+            const int64_t Lq = cu_q[b + 1] - q0, Lk = cu_k[b + 1] - k0;
+            if (Lq < 0 || Lk < 0) { bad |= 1; continue; }
+            const int64_t n = Lk > 0 ? Lk : 1;
+            double* qrow = (double*)malloc(sizeof(double) * d);
+            double* dorow = (double*)malloc(sizeof(double) * d);
+            double* kbuf = (double*)malloc(sizeof(double) * d);
+            double* s_row = (double*)malloc(sizeof(double) * n);
+            double* p_row = (double*)malloc(sizeof(double) * n);
+            double* dp_row = (double*)malloc(sizeof(double) * n);
+            for (int64_t i = 0; i < Lq; ++i) {
+                for (int hh = 0; hh < g; ++hh) {
+                    const int h = kvh * g + hh;
+                    const int64_t t = q0 + i;
+                    load_row(q, dtype, (t * Hq + h) * d, d, qrow);
+                    load_row(dout, dtype, (t * Hq + h) * d, d, dorow);
+                    /* S and P rows */
+                    double m = -INFINITY;
+                    for (int64_t j = 0; j < Lk; ++j) {
+                        if (!oracle_allowed(i, j, Lq, Lk, causal, wl, wr)) { s_row[j] = -INFINITY; continue; }
+                        load_row(k, dtype, ((k0 + j) * Hkv + kvh) * d, d, kbuf);
+                        double acc = 0.0;
+                        for (int e = 0; e < d; ++e) acc += qrow[e] * kbuf[e];
+                        s_row[j] = scale * acc;
+                        if (s_row[j] > m) m = s_row[j];
+                    }
+                    if (m == -INFINITY) {          /* no visible key: O = 0, no gradient */
+                        dsum[(int64_t)h * total_q + t] = 0.0;
+                        continue;
+                    }
+                    double denom = 0.0;
+                    for (int64_t j = 0; j < Lk; ++j) {
+                        p_row[j] = s_row[j] == -INFINITY ? 0.0 : exp(s_row[j] - m);
+                        denom += p_row[j];
+                    }
+                    for (int64_t j = 0; j < Lk; ++j) p_row[j] /= denom;
+                    /* dP row, D_i */
+                    double D = 0.0;
+                    for (int64_t j = 0; j < Lk; ++j) {
+                        if (p_row[j] == 0.0) { dp_row[j] = 0.0; continue; }
+                        load_row(v, dtype, ((k0 + j) * Hkv + kvh) * d, d, kbuf);
+                        double acc = 0.0;
+                        for (int e = 0; e < d; ++e) acc += dorow[e] * kbuf[e];
+                        dp_row[j] = acc;
+                        D += p_row[j] * acc;
+                    }
+                    dsum[(int64_t)h * total_q + t] = D;
+                    /* dS = P (dP - D); dQ_i, dK_j, dV_j */
+                    double* dqrow = dq + (t * Hq + h) * d;
+                    for (int64_t j = 0; j < Lk; ++j) {
+                        if (p_row[j] == 0.0) continue;
+                        const double ds = p_row[j] * (dp_row[j] - D);
+                        const int64_t kv = ((k0 + j) * Hkv + kvh) * d;
+                        load_row(k, dtype, kv, d, kbuf);
+                        for (int e = 0; e < d; ++e) dqrow[e] += scale * ds * kbuf[e];
+                        for (int e = 0; e < d; ++e) {
+                            dk[kv + e] += scale * ds * qrow[e];
+                            dv[kv + e] += p_row[j] * dorow[e];
+                        }
+                    }
+                }
+            }
+            free(qrow); free(dorow); free(kbuf); free(s_row); free(p_row); free(dp_row);
+        }
+    }
+    return bad ? -1 : 0;
+}
+
 /* ---- chunked prefill over a paged cache, with KV append and rotary embedding ---------- */
 
 /*

@@ -75,6 +75,9 @@ def _load():
             lib.oracle_tiled_traffic_bytes.argtypes = [ll, ll, ll]
             lib.oracle_num_threads.restype = i32
             lib.oracle_num_threads.argtypes = []
+            lib.oracle_attn_bwd.restype = i32
+            lib.oracle_attn_bwd.argtypes = [P, P, P, P, i32, P, P, i32, i32, i32, i32, dbl, i32,
+                                            i32, i32, P, P, P, P]
             lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
             lib.oracle_f64_to_bf16.argtypes = [dbl]
             lib.oracle_kvcache_prefill.restype = i32
@@ -226,6 +229,33 @@ def decode(q, k_cache, v_cache, cache_seqlens, block_table, softmax_scale, num_s
     if rows_b is None:
         return out.reshape(batch, Hq, d), lse.reshape(batch, Hq)
     return out, lse
+
+
+def attn_bwd(q, k, v, dout, cu_seqlens_q, cu_seqlens_k, softmax_scale, causal=False,
+             window_left=-1, window_right=-1):
+    """Gradients of sum(O * dout) for attn_fwd's attention.
+
+    Returns (dq [total_q, Hq, d], dk [total_k, Hkv, d], dv [total_k, Hkv, d],
+    D [Hq, total_q] = rowsum(dout * O)), all fp64.
+    """
+    qa, dt = _host(q)
+    ka, _ = _host(k)
+    va, _ = _host(v)
+    da, _ = _host(dout)
+    total_q, Hq, d = qa.shape
+    total_k, Hkv = ka.shape[0], ka.shape[1]
+    cu_q, cu_k = _i32(cu_seqlens_q), _i32(cu_seqlens_k)
+    dq = np.zeros((total_q, Hq, d), np.float64)
+    dk = np.zeros((total_k, Hkv, d), np.float64)
+    dv = np.zeros((total_k, Hkv, d), np.float64)
+    D = np.zeros((Hq, total_q), np.float64)
+    rc = _load().oracle_attn_bwd(_ptr(qa), _ptr(ka), _ptr(va), _ptr(da), dt, _ptr(cu_q),
+                                 _ptr(cu_k), len(cu_q) - 1, Hq, Hkv, d, float(softmax_scale),
+                                 int(causal), window_left, window_right, _ptr(dq), _ptr(dk),
+                                 _ptr(dv), _ptr(D))
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd rejected its arguments")
+    return dq, dk, dv, D
 
 
 def f64_to_bf16_bits(x: float) -> int:
