@@ -63,6 +63,10 @@ def load():
             lib.attn_fwd_kvcache.argtypes = [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, P, P,
                                              i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                              ctypes.c_float, i32, i32, i32, P, sz, P]
+            lib.attn_bwd.restype = i32
+            lib.attn_bwd.argtypes = [P] * 11 + [i32] * 8 + [f32, i32, i32, i32, P, sz, P]
+            lib.attn_bwd_workspace_bytes.restype = sz
+            lib.attn_bwd_workspace_bytes.argtypes = [i32, i32]
             lib.attn_fwd_kvcache_workspace_bytes.restype = sz
             lib.attn_fwd_kvcache_workspace_bytes.argtypes = [i32] * 7
             lib.attn_status_string.restype = ctypes.c_char_p
@@ -182,6 +186,35 @@ def attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
     if rc != 0:
         raise AttnError(rc, "attn_fwd")
     return out, lse
+
+
+def attn_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+             softmax_scale=None, causal=False, window_left=-1, window_right=-1, dq=None,
+             dk=None, dv=None, workspace=None, stream=None):
+    """Gradients of sum(out * dout) for attn_fwd.  Returns (dq, dk, dv), bf16."""
+    lib = load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _check(t, n, torch.bfloat16, 3)
+    _check(lse, "lse", torch.float32, 2)
+    _check(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _check(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    total_q, Hq, d = q.shape
+    total_k, Hkv, _ = k.shape
+    batch = cu_seqlens_q.numel() - 1
+    scale = d ** -0.5 if softmax_scale is None else float(softmax_scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    nbytes = int(lib.attn_bwd_workspace_bytes(total_q, Hq))
+    ws = _workspace(nbytes, q.device, workspace)
+    rc = lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq),
+                      _ptr(dk), _ptr(dv), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, total_q,
+                      total_k, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, d, scale,
+                      int(bool(causal)), int(window_left), int(window_right), _ptr(ws), nbytes,
+                      _stream(stream))
+    if rc != 0:
+        raise AttnError(rc, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_fwd_kvcache(q, k_new, v_new, k_cache, v_cache, cache_seqlens, block_table,

@@ -379,6 +379,84 @@ attn_status_t attn_fwd_kvcache(const void* q, const void* k_new, const void* v_n
     return ATTN_OK;
 }
 
+size_t attn_bwd_workspace_bytes(int total_q, int nheads_q) {
+    if (total_q < 0 || nheads_q <= 0) return 0;
+    return align_up(static_cast<size_t>(total_q) * nheads_q * sizeof(float), 256);
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch,
+                       int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                       int nheads_q, int nheads_kv, int head_dim, float softmax_scale,
+                       int causal, int window_left, int window_right, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+    if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
+        nheads_q <= 0 || nheads_kv <= 0 || window_left < -1 || window_right < -1 ||
+        !scale_ok(softmax_scale))
+        return ATTN_ERR_INVALID_ARG;
+    if (nheads_q % nheads_kv != 0) return ATTN_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+    const int g = nheads_q / nheads_kv;
+    if (g > 128) return ATTN_ERR_UNSUPPORTED;
+    if (batch == 0 || (total_q == 0 && total_k == 0)) return ATTN_OK;
+    if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv || !cu_seqlens_q ||
+        !cu_seqlens_k)
+        return ATTN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+        !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+        !aligned(lse, 4) || !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4))
+        return ATTN_ERR_INVALID_ARG;
+    if (static_cast<long long>(total_q) * nheads_q > (1LL << 31) - 1 ||
+        static_cast<long long>(total_k) * nheads_kv > (1LL << 31) - 1 ||
+        static_cast<long long>(batch) * nheads_kv > 65535)
+        return ATTN_ERR_UNSUPPORTED;
+    const size_t need = attn_bwd_workspace_bytes(total_q, nheads_q);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
+        return ATTN_ERR_WORKSPACE;
+
+    DeviceState* dev = nullptr;
+    attn_status_t st = device_state(&dev);
+    if (st != ATTN_OK) return st;
+
+    const int tpt = tokens_per_tile(g);
+    BwdParams bp;
+    memset(&bp, 0, sizeof(bp));
+    if (encode_3d(&bp.tm_q, q, head_dim, nheads_q, total_q > 0 ? total_q : 1, g, tpt) != ATTN_OK ||
+        encode_3d(&bp.tm_do, dout, head_dim, nheads_q, total_q > 0 ? total_q : 1, g, tpt) != ATTN_OK ||
+        encode_3d(&bp.tm_k, k, head_dim, nheads_kv, total_k > 0 ? total_k : 1, 1, 128) != ATTN_OK ||
+        encode_3d(&bp.tm_v, v, head_dim, nheads_kv, total_k > 0 ? total_k : 1, 1, 128) != ATTN_OK)
+        return ATTN_ERR_CUDA;
+    bp.o = static_cast<const __nv_bfloat16*>(out);
+    bp.dout = static_cast<const __nv_bfloat16*>(dout);
+    bp.lse = lse;
+    bp.dsum = static_cast<float*>(workspace);
+    bp.dq = static_cast<__nv_bfloat16*>(dq);
+    bp.dk = static_cast<__nv_bfloat16*>(dk);
+    bp.dv = static_cast<__nv_bfloat16*>(dv);
+    bp.cu_q = cu_seqlens_q;
+    bp.cu_k = cu_seqlens_k;
+    bp.status = dev->status;
+    bp.batch = batch;
+    bp.Hq = nheads_q;
+    bp.Hkv = nheads_kv;
+    bp.g = g;
+    bp.tpt = tpt;
+    bp.total_q = total_q;
+    bp.total_k = total_k;
+    bp.d = head_dim;
+    bp.max_seqlen_q = max_seqlen_q;
+    bp.max_seqlen_k = max_seqlen_k;
+    bp.causal = causal ? 1 : 0;
+    bp.wl = window_left;
+    bp.wr = window_right;
+    bp.scale = softmax_scale;
+    bp.scale_log2 = softmax_scale * kLog2eF;
+    if (launch_bwd(bp, dev->num_sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
 int attn_decode_num_splits(int batch, int nheads_q, int nheads_kv, int max_pages_per_seq,
                            int page_size, int num_sms) {
     if (batch <= 0 || nheads_q <= 0 || nheads_kv <= 0 || nheads_q % nheads_kv != 0 ||

@@ -88,6 +88,30 @@ cudaError_t launch_fwd_prepare(const FwdPrepParams& p, cudaStream_t stream);
 cudaError_t launch_fwd(const FwdParams& p, int head_dim, int grid, cudaStream_t stream);
 int fwd_smem_bytes(int head_dim);
 
+// ---- backward ------------------------------------------------------------------------------
+
+struct BwdParams {
+    CUtensorMap tm_q;   // 3-D over q    [total_q, Hq, d], box {64, g, tpt}
+    CUtensorMap tm_do;  // 3-D over dout [total_q, Hq, d], box {64, g, tpt}
+    CUtensorMap tm_k;   // 3-D over k    [total_k, Hkv, d], box {64, 1, 128}
+    CUtensorMap tm_v;
+    const __nv_bfloat16* o;     // [total_q, Hq, d]
+    const __nv_bfloat16* dout;
+    const float* lse;           // [Hq, total_q]
+    float* dsum;                // [Hq, total_q]: D = rowsum(dout * o)
+    __nv_bfloat16* dq;          // [total_q, Hq, d]
+    __nv_bfloat16* dk;          // [total_k, Hkv, d]
+    __nv_bfloat16* dv;
+    const int* cu_q;
+    const int* cu_k;
+    unsigned* status;
+    int batch, Hq, Hkv, g, tpt, total_q, total_k, d, max_seqlen_q, max_seqlen_k;
+    int causal, wl, wr;
+    float scale, scale_log2;
+};
+
+cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t stream);
+
 // ---- failure-path self-test ------------------------------------------------------------
 
 cudaError_t launch_watchdog_selftest(unsigned* status, cudaStream_t stream);

@@ -195,6 +195,34 @@ attn_status_t attn_fwd_kvcache(const void* q, const void* k_new, const void* v_n
 size_t attn_fwd_kvcache_workspace_bytes(int batch, int total_q, int max_seqlen_q, int nheads_q,
                                         int nheads_kv, int head_dim, int rotary_dim);
 
+/*
+ * Backward pass of attn_fwd: gradients of sum(out * dout) with respect to q, k and v
+ * ("Attention kernels: FlashAttention and PagedAttention", section 四.3: S = Q K^T and
+ * P = exp(S - LSE) are recomputed blockwise from the saved LSE; D = rowsum(dout * out);
+ * dV = P^T dout, dS = P * (dout V^T - D), dQ = scale dS K, dK = scale dS^T Q; a kv head's
+ * dK, dV sum over its query heads).  dQ of a row is accumulated inside one CTA, so results do
+ * not depend on scheduling (no atomics).
+ *
+ *   q, out, dout, dq  bf16 [total_q, nheads_q, head_dim]
+ *   k, v, dk, dv      bf16 [total_k, nheads_kv, head_dim]
+ *   lse               fp32 [nheads_q, total_q] from attn_fwd (natural log)
+ *   the remaining arguments as in attn_fwd (same sequences, mask, window and scale).
+ *   workspace: attn_bwd_workspace_bytes(total_q, nheads_q) bytes, 256-byte aligned (D).
+ * Rows without a visible key get zero gradient; keys no row sees get dk = dv = 0.
+ * Ownership: caller's buffers.  Errors: argument checks before any launch; inconsistent
+ * cu_seqlens raise ATTN_ERR_DEVICE_BOUNDS.
+ */
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch,
+                       int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                       int nheads_q, int nheads_kv, int head_dim, float softmax_scale,
+                       int causal, int window_left, int window_right, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/* Workspace bytes for attn_bwd (D, fp32 per (head, token)). */
+size_t attn_bwd_workspace_bytes(int total_q, int nheads_q);
+
 /* Bytes of split-partial workspace for attn_decode_kvcache; num_splits 0 sizes for the
  * automatic choice (at most 16 splits).  0 when one split needs no workspace. */
 size_t attn_decode_workspace_bytes(int batch, int nheads_q, int head_dim, int num_splits);

@@ -184,3 +184,25 @@ def test_kvcache_arguments_are_rejected_before_any_launch(lib):
     assert lib.attn_fwd_kvcache_workspace_bytes(2, 16, 8, 8, 2, 128, 0) == (base + 255) // 256 * 256
     assert lib.attn_fwd_kvcache_workspace_bytes(2, 16, 8, 8, 2, 128, 64) == \
         (base + 255) // 256 * 256 + 16 * 8 * 128 * 2
+
+
+def test_bwd_arguments_are_rejected_before_any_launch(lib):
+    P = ctypes.c_void_p
+    fake = P(4096)
+    f = lib.attn_bwd
+    args = [fake] * 11 + [1, 16, 16, 16, 16, 4, 2, 128, 0.1, 1, -1, -1, fake, 1 << 20, None]
+
+    def call(i, v):
+        a = list(args)
+        a[i] = v
+        return f(*a)
+
+    assert call(17, 3) == -1       # Hq % Hkv
+    assert call(18, 96) == -2      # head_dim
+    assert call(19, 0.0) == -1     # scale
+    assert call(0, None) == -1     # q
+    assert call(4, P(4100)) == -1  # misaligned dout
+    assert call(23, None) == -3    # workspace
+    assert call(11, 0) == 0        # batch 0
+    assert lib.attn_bwd_workspace_bytes(1000, 8) == (32000 + 255) // 256 * 256
+    assert lib.attn_bwd_workspace_bytes(1001, 8) == (32032 + 255) // 256 * 256
