@@ -392,6 +392,34 @@ def run_ours(args, rank, world, local):
         extra["chunked"] = {"workload": synth.CHUNKED_NAME, "ms": round(ms, 4),
                             "tflops": round(fl / ms / 1e9, 2)}
         del t, co
+        # backward of the causal prefill workload (gradients of q, k, v)
+        c = synth.config_case(2)
+        bq, bk, bv = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+        bcq, bck = c.cu_seqlens_q.to(dev), c.cu_seqlens_k.to(dev)
+        bo, bl = binding.attn_fwd(bq, bk, bv, bcq, bck, c.max_seqlen_q, c.max_seqlen_k,
+                                  c.softmax_scale, True)
+        bdo = synth.randn_bf16(tuple(c.q.shape), 1200, 9).to(dev)
+        gq, gk, gv = torch.empty_like(bq), torch.empty_like(bk), torch.empty_like(bv)
+        bws = torch.empty(binding.attn_bwd_workspace_bytes(bq.shape[0], bq.shape[1]),
+                          dtype=torch.uint8, device=dev)
+
+        def run_b():
+            binding.attn_bwd(bq, bk, bv, bo, bdo, bl, bcq, bck, c.max_seqlen_q, c.max_seqlen_k,
+                             c.softmax_scale, True, dq=gq, dk=gk, dv=gv, workspace=bws)
+        for _ in range(3):
+            run_b()
+        reps = 10
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            run_b()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        fl = workload.prefill_case_flops(c) * 10 // 4   # S, dP, dV, dK, dQ: 10 d per pair
+        extra["bwd"] = {"workload": "backward of " + synth.CONFIG_NAMES[2], "ms": round(ms, 4),
+                        "tflops": round(fl / ms / 1e9, 2)}
+        del bq, bk, bv, bo, bdo, gq, gk, gv
     return dict(p_flops=p_flops, d_bytes=d_bytes, total_ms=total_ms, pre_ms=pre_ms,
                 dec_ms=dec_ms, e2e_pre=e2e_pre, e2e_dec=e2e_dec, h2d_pre=h2d_pre,
                 d2h_pre=d2h_pre, h2d_dec=h2d_dec, d2h_dec=d2h_dec, clocks=clk, splits=splits,

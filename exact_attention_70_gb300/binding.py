@@ -103,6 +103,10 @@ def _check(t, name, dtype, ndim):
         raise ValueError(f"{name} must be contiguous")
 
 
+def attn_bwd_workspace_bytes(total_q, nheads_q) -> int:
+    return int(load().attn_bwd_workspace_bytes(int(total_q), int(nheads_q)))
+
+
 def attn_fwd_workspace_bytes(batch, max_seqlen_q, nheads_q, nheads_kv) -> int:
     return int(load().attn_fwd_workspace_bytes(batch, max_seqlen_q, nheads_q, nheads_kv))
 

@@ -2,11 +2,11 @@
 
 The GPU forward produces out and lse; a seeded bf16 dout drives the GPU backward and the
 oracle (which recomputes everything in fp64 from q, k, v, dout).  Tolerance, per gradient
-tensor, relative to its own scale: max |err| <= 3e-2 * max |ref| and mean |err| <= 1e-2 *
-mean |ref|.  Sources of difference: P and dS enter the tensor-core products as bf16 (relative
+tensor, relative to its own scale: max |err| <= 2e-2 * max |ref| and mean |err| <= 5e-3 *
+mean |ref| (observed: at most 0.8e-2 and 0.25e-2).  Sources of difference: P and dS enter the tensor-core products as bf16 (relative
 rounding 2^-9 each), dout V^T and the products accumulate in fp32, D uses the bf16 forward
 output, and the gradients are rounded to bf16 (2^-9); with hundreds of terms per element the
-errors add like a random walk, leaving the typical element near 1e-2 relative.
+errors add like a random walk, leaving the typical element a few 1e-3 relative.
 """
 import numpy as np
 import pytest
@@ -34,8 +34,8 @@ def check_grad(gpu, ref, what):
     err = np.abs(g - ref)
     scale_max, scale_mean = np.abs(ref).max(), np.abs(ref).mean()
     assert np.all(np.isfinite(g)), what
-    assert err.max() <= 3e-2 * scale_max + 1e-6, (what, err.max(), scale_max)
-    assert err.mean() <= 1e-2 * scale_mean + 1e-7, (what, err.mean(), scale_mean)
+    assert err.max() <= 2e-2 * scale_max + 1e-6, (what, err.max(), scale_max)
+    assert err.mean() <= 5e-3 * scale_mean + 1e-7, (what, err.mean(), scale_mean)
 
 
 def run_case(attn, case, seed):
