@@ -89,11 +89,19 @@ int oracle_allowed(long long i, long long j, long long Lq, long long Lk, int cau
  * are koff[0..Lk) (the same offsets index V), then form O and the row's LSE.
  * vis[j] != 0 marks visible keys.  s_row and p_row are caller scratch of Lk doubles.
  */
+/* Optional score modifiers ("04 · FA4 ...", section 7): softcap s -> c tanh(s / c) of the
+ * scaled score, then the ALiBi bias -slope |pos - j| with pos the query's key position. */
+typedef struct {
+    double softcap;  /* 0: off */
+    double slope;    /* 0: no ALiBi */
+    int64_t pos;
+} score_mod_t;
+
 static void attention_row(const double* qrow, const void* k, const void* v, int dtype,
                           const int64_t* koff, const unsigned char* vis, int64_t Lk, int d,
                           double scale, double* s_row, double* p_row, double* kbuf,
-                          double* out, double* lse, long long* pairs) {
-    /* S row: s_j = scale * <q, k_j> for visible keys, -inf otherwise. */
+                          double* out, double* lse, long long* pairs, const score_mod_t* mod) {
+    /* S row: s_j = scale * <q, k_j> (then the modifiers) for visible keys, -inf otherwise. */
     long long visible = 0;
     for (int64_t j = 0; j < Lk; ++j) {
         if (!vis[j]) { s_row[j] = -INFINITY; continue; }
@@ -101,6 +109,10 @@ static void attention_row(const double* qrow, const void* k, const void* v, int 
         double acc = 0.0;
         for (int e = 0; e < d; ++e) acc += qrow[e] * kbuf[e];
         s_row[j] = scale * acc;
+        if (mod) {
+            if (mod->softcap > 0.0) s_row[j] = mod->softcap * tanh(s_row[j] / mod->softcap);
+            if (mod->slope != 0.0) s_row[j] -= mod->slope * fabs((double)(mod->pos - j));
+        }
         ++visible;
     }
     if (pairs) *pairs += visible;
@@ -180,7 +192,7 @@ int oracle_attn_fwd(const void* q, const void* k, const void* v, int dtype,
             load_row(q, dtype, (t * Hq + h) * d, d, qrow);
             long long pairs = 0;
             attention_row(qrow, k, v, dtype, koff, vis, Lk, d, scale, s_row, p_row, kbuf,
-                          out + (t * Hq + h) * d, lse + (int64_t)h * total_q + t, &pairs);
+                          out + (t * Hq + h) * d, lse + (int64_t)h * total_q + t, &pairs, NULL);
             flops += 4LL * d * pairs;
             s_el += Lk;
             p_el += Lk;
@@ -228,7 +240,7 @@ int oracle_attn_fwd_rows(const void* q, const void* k, const void* v, int dtype,
         }
         load_row(q, dtype, (t * Hq + h) * d, d, qrow);
         attention_row(qrow, k, v, dtype, koff, vis, Lk, d, scale, s_row, p_row, kbuf,
-                      out + r * d, lse + r, NULL);
+                      out + r * d, lse + r, NULL, NULL);
         free(koff); free(vis); free(s_row); free(p_row); free(qrow); free(kbuf);
     }
     return bad ? -1 : 0;
@@ -312,7 +324,7 @@ int oracle_decode(const void* q, const void* k_cache, const void* v_cache, int d
             for (int64_t j = 0; j < L; ++j)
                 vis[j] = (unsigned char)oracle_allowed(0, j, 1, L, 1, -1, -1);
             attention_row(qrow, k_cache, v_cache, dtype, koff, vis, L, d, scale, s_row, p_row,
-                          kbuf, out + r * d, lse + r, NULL);
+                          kbuf, out + r * d, lse + r, NULL, NULL);
         } else {
             const int S = num_splits;
             const int64_t C = (L + S - 1) / S;
@@ -327,7 +339,7 @@ int oracle_decode(const void* q, const void* k_cache, const void* v_cache, int d
                     vis[j] = (unsigned char)oracle_allowed(0, j0 + j, 1, L, 1, -1, -1);
                 double lse_s;
                 attention_row(qrow, k_cache, v_cache, dtype, koff + j0, vis, n_s, d, scale,
-                              s_row, p_row, kbuf, o_i + (int64_t)s * d, &lse_s, NULL);
+                              s_row, p_row, kbuf, o_i + (int64_t)s * d, &lse_s, NULL, NULL);
                 /* express the partial as (m_s, l_s) with O_s normalised */
                 if (lse_s == -INFINITY) { m_i[s] = -INFINITY; l_i[s] = 0.0; }
                 else {
@@ -344,6 +356,55 @@ int oracle_decode(const void* q, const void* k_cache, const void* v_cache, int d
             free(m_i); free(l_i); free(o_i);
         }
         free(koff); free(qrow); free(kbuf); free(s_row); free(p_row); free(vis);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * Standard attention with the score modifiers of "04 · FA4 ...", section 7: softcap
+ * (s -> c tanh(s / c) on the scaled score; c = 0 off) and ALiBi (a linear position bias,
+ * here -slope_h |i + Lk - Lq - j|; slopes == NULL off), then the visibility mask and softmax.
+ * Rows are (packed token, q head) pairs; rows_t == NULL means all total_q * Hq rows in
+ * (token, head) order.  out [nrows, d], lse [nrows].
+ */
+int oracle_attn_fwd_mods(const void* q, const void* k, const void* v, int dtype,
+                         const int32_t* cu_q, const int32_t* cu_k, int batch, int Hq, int Hkv,
+                         int d, double scale, int causal, int wl, int wr, double softcap,
+                         const double* slopes, const int64_t* rows_t, const int32_t* rows_h,
+                         long long nrows, double* out, double* lse) {
+    if (check_common(batch, Hq, Hkv, d) || softcap < 0.0) return -1;
+    const int g = Hq / Hkv;
+    const int64_t total_q = cu_q[batch];
+    const long long n = rows_t ? nrows : total_q * Hq;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 8) reduction(| : bad)
+    for (long long r = 0; r < n; ++r) {
+        const int64_t t = rows_t ? rows_t[r] : r / Hq;
+        const int h = rows_t ? rows_h[r] : (int)(r % Hq);
+        if (t < 0 || t >= total_q || h < 0 || h >= Hq) { bad |= 1; continue; }
+        const int b = find_seq(cu_q, batch, t);
+        const int64_t i = t - cu_q[b];
+        const int64_t Lq = (int64_t)cu_q[b + 1] - cu_q[b];
+        const int64_t k0 = cu_k[b], Lk = (int64_t)cu_k[b + 1] - k0;
+        const int kvh = h / g;
+        double* qrow = (double*)malloc(sizeof(double) * d);
+        double* kbuf = (double*)malloc(sizeof(double) * d);
+        int64_t* koff = (int64_t*)malloc(sizeof(int64_t) * (Lk > 0 ? Lk : 1));
+        double* s_row = (double*)malloc(sizeof(double) * (Lk > 0 ? Lk : 1));
+        double* p_row = (double*)malloc(sizeof(double) * (Lk > 0 ? Lk : 1));
+        unsigned char* vis = (unsigned char*)malloc(Lk > 0 ? Lk : 1);
+        load_row(q, dtype, (t * Hq + h) * d, d, qrow);
+        for (int64_t j = 0; j < Lk; ++j) {
+            koff[j] = ((k0 + j) * Hkv + kvh) * d;
+            vis[j] = (unsigned char)oracle_allowed(i, j, Lq, Lk, causal, wl, wr);
+        }
+        score_mod_t mod;
+        mod.softcap = softcap;
+        mod.slope = slopes ? slopes[h] : 0.0;
+        mod.pos = i + Lk - Lq;
+        attention_row(qrow, k, v, dtype, koff, vis, Lk, d, scale, s_row, p_row, kbuf,
+                      out + r * d, lse + r, NULL, &mod);
+        free(qrow); free(kbuf); free(koff); free(s_row); free(p_row); free(vis);
     }
     return bad ? -1 : 0;
 }
@@ -590,7 +651,7 @@ int oracle_kvcache_prefill(const void* q, const void* k_new, const void* v_new, 
             vis[j] = (unsigned char)oracle_allowed(i, j, Lq, Lk, causal, wl, wr);
         }
         attention_row(qrow, k_cache, v_cache, dtype, koff, vis, Lk, d, scale, s_row, p_row, kbuf,
-                      out + r * d, lse + r, NULL);
+                      out + r * d, lse + r, NULL, NULL);
         free(qrow); free(kbuf); free(koff); free(s_row); free(p_row); free(vis);
     }
     return bad ? -1 : 0;

@@ -75,6 +75,9 @@ def _load():
             lib.oracle_tiled_traffic_bytes.argtypes = [ll, ll, ll]
             lib.oracle_num_threads.restype = i32
             lib.oracle_num_threads.argtypes = []
+            lib.oracle_attn_fwd_mods.restype = i32
+            lib.oracle_attn_fwd_mods.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, dbl,
+                                                 i32, i32, i32, dbl, P, P, P, ll, P, P]
             lib.oracle_attn_bwd.restype = i32
             lib.oracle_attn_bwd.argtypes = [P, P, P, P, i32, P, P, i32, i32, i32, i32, dbl, i32,
                                             i32, i32, P, P, P, P]
@@ -228,6 +231,42 @@ def decode(q, k_cache, v_cache, cache_seqlens, block_table, softmax_scale, num_s
         raise ValueError("oracle_decode rejected its arguments (bad page index or length)")
     if rows_b is None:
         return out.reshape(batch, Hq, d), lse.reshape(batch, Hq)
+    return out, lse
+
+
+def attn_fwd_mods(q, k, v, cu_seqlens_q, cu_seqlens_k, softmax_scale, causal=False,
+                  window_left=-1, window_right=-1, softcap=0.0, alibi_slopes=None,
+                  rows_t=None, rows_h=None):
+    """attn_fwd with the softcap and ALiBi score modifiers.
+
+    Returns (out, lse): [n, d] and [n] for chosen (token, head) rows, or
+    [total_q, Hq, d] and [Hq, total_q] for all rows.
+    """
+    qa, dt = _host(q)
+    ka, _ = _host(k)
+    va, _ = _host(v)
+    total_q, Hq, d = qa.shape
+    Hkv = ka.shape[1]
+    cu_q, cu_k = _i32(cu_seqlens_q), _i32(cu_seqlens_k)
+    sl = None if alibi_slopes is None else np.ascontiguousarray(np.asarray(alibi_slopes, dtype=np.float64))
+    if rows_t is None:
+        n, rt, rh = total_q * Hq, None, None
+    else:
+        rt = np.ascontiguousarray(np.asarray(rows_t), dtype=np.int64)
+        rh = np.ascontiguousarray(np.asarray(rows_h), dtype=np.int32)
+        n = len(rt)
+    out = np.zeros((n, d), np.float64)
+    lse = np.zeros((n,), np.float64)
+    rc = _load().oracle_attn_fwd_mods(_ptr(qa), _ptr(ka), _ptr(va), dt, _ptr(cu_q), _ptr(cu_k),
+                                      len(cu_q) - 1, Hq, Hkv, d, float(softmax_scale), int(causal),
+                                      window_left, window_right, float(softcap),
+                                      _ptr(sl) if sl is not None else None,
+                                      _ptr(rt) if rt is not None else None,
+                                      _ptr(rh) if rh is not None else None, n, _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle_attn_fwd_mods rejected its arguments")
+    if rows_t is None:
+        return out.reshape(total_q, Hq, d), lse.reshape(total_q, Hq).T.copy()
     return out, lse
 
 
