@@ -392,6 +392,33 @@ def run_ours(args, rank, world, local):
         extra["chunked"] = {"workload": synth.CHUNKED_NAME, "ms": round(ms, 4),
                             "tflops": round(fl / ms / 1e9, 2)}
         del t, co
+        # the causal prefill workload with both score modifiers (softcap 30, ALiBi slopes)
+        c = synth.config_case(2)
+        mq, mk, mv = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+        mcq, mck = c.cu_seqlens_q.to(dev), c.cu_seqlens_k.to(dev)
+        Hq = mq.shape[1]
+        slopes = torch.tensor([2.0 ** (-8.0 * (h + 1) / Hq) for h in range(Hq)],
+                              dtype=torch.float32, device=dev)
+        mo, ml = torch.empty_like(mq), torch.empty((Hq, mq.shape[0]), dtype=torch.float32, device=dev)
+
+        def run_m():
+            binding.attn_fwd_mods(mq, mk, mv, mcq, mck, c.max_seqlen_q, c.max_seqlen_k,
+                                  c.softmax_scale, True, softcap=30.0, alibi_slopes=slopes,
+                                  out=mo, lse=ml)
+        for _ in range(3):
+            run_m()
+        reps = 10
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            run_m()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        extra["mods"] = {"workload": synth.CONFIG_NAMES[2] + " with softcap 30 and ALiBi",
+                         "ms": round(ms, 4),
+                         "tflops": round(workload.prefill_case_flops(c) / ms / 1e9, 2)}
+        del mq, mk, mv, mo
         # backward of the causal prefill workload (gradients of q, k, v)
         c = synth.config_case(2)
         bq, bk, bv = c.q.to(dev), c.k.to(dev), c.v.to(dev)

@@ -63,6 +63,9 @@ def load():
             lib.attn_fwd_kvcache.argtypes = [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, P, P,
                                              i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                              ctypes.c_float, i32, i32, i32, P, sz, P]
+            lib.attn_fwd_mods.restype = i32
+            lib.attn_fwd_mods.argtypes = [P, P, P, P, P, P, P] + [i32] * 8 + [f32, i32, i32, i32,
+                                                                            f32, P, P, sz, P]
             lib.attn_bwd.restype = i32
             lib.attn_bwd.argtypes = [P] * 11 + [i32] * 8 + [f32, i32, i32, i32, P, sz, P]
             lib.attn_bwd_workspace_bytes.restype = sz
@@ -189,6 +192,35 @@ def attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
                       int(window_right), _ptr(ws), nbytes, _stream(stream))
     if rc != 0:
         raise AttnError(rc, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_mods(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                  softmax_scale=None, causal=False, window_left=-1, window_right=-1,
+                  softcap=0.0, alibi_slopes=None, out=None, lse=None, workspace=None,
+                  stream=None):
+    """attn_fwd with softcap (0 = off) and ALiBi slopes (fp32 [Hq] CUDA tensor or None)."""
+    lib = load()
+    _check(q, "q", torch.bfloat16, 3)
+    _check(k, "k", torch.bfloat16, 3)
+    _check(v, "v", torch.bfloat16, 3)
+    if alibi_slopes is not None:
+        _check(alibi_slopes, "alibi_slopes", torch.float32, 1)
+    total_q, Hq, d = q.shape
+    total_k, Hkv, _ = k.shape
+    batch = cu_seqlens_q.numel() - 1
+    scale = d ** -0.5 if softmax_scale is None else float(softmax_scale)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device) if lse is None else lse
+    nbytes = int(lib.attn_fwd_workspace_bytes(max(batch, 0), int(max_seqlen_q), Hq, Hkv))
+    ws = _workspace(nbytes, q.device, workspace)
+    rc = lib.attn_fwd_mods(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q),
+                           _ptr(cu_seqlens_k), batch, total_q, total_k, int(max_seqlen_q),
+                           int(max_seqlen_k), Hq, Hkv, d, scale, int(bool(causal)),
+                           int(window_left), int(window_right), float(softcap),
+                           _ptr(alibi_slopes), _ptr(ws), nbytes, _stream(stream))
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd_mods")
     return out, lse
 
 

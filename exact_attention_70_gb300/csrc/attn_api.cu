@@ -133,12 +133,19 @@ int attn_kv_block_masked(int j, int i_min, int i_max, int seqlen_q, int seqlen_k
                : 0;
 }
 
-attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+}  // extern "C"
+
+namespace {
+
+attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse,
                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch,
                        int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
                        int nheads_q, int nheads_kv, int head_dim, float softmax_scale,
                        int causal, int window_left, int window_right, void* workspace,
-                       size_t workspace_bytes, void* stream) {
+                       size_t workspace_bytes, void* stream, float softcap,
+                       const float* alibi_slopes) {
+    if (!(softcap >= 0.f) || softcap > 1e30f || (alibi_slopes && !aligned(alibi_slopes, 4)))
+        return ATTN_ERR_INVALID_ARG;
     if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
         nheads_q <= 0 || nheads_kv <= 0 || window_left < -1 || window_right < -1 ||
         !scale_ok(softmax_scale))
@@ -219,10 +226,42 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* out, f
     fp.wl = window_left;
     fp.wr = window_right;
     fp.scale_log2 = softmax_scale * kLog2eF;
+    fp.scale = softmax_scale;
+    fp.softcap = softcap;
+    fp.alibi = alibi_slopes;
 
     if (launch_fwd_prepare(pp, s) != cudaSuccess) return ATTN_ERR_CUDA;
     if (launch_fwd(fp, head_dim, dev->num_sms, s) != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch,
+                       int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                       int nheads_q, int nheads_kv, int head_dim, float softmax_scale,
+                       int causal, int window_left, int window_right, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+    return fwd_impl(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
+                    max_seqlen_q, max_seqlen_k, nheads_q, nheads_kv, head_dim, softmax_scale,
+                    causal, window_left, window_right, workspace, workspace_bytes, stream, 0.f,
+                    nullptr);
+}
+
+attn_status_t attn_fwd_mods(const void* q, const void* k, const void* v, void* out, float* lse,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch,
+                            int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                            int nheads_q, int nheads_kv, int head_dim, float softmax_scale,
+                            int causal, int window_left, int window_right, float softcap,
+                            const float* alibi_slopes, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+    return fwd_impl(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
+                    max_seqlen_q, max_seqlen_k, nheads_q, nheads_kv, head_dim, softmax_scale,
+                    causal, window_left, window_right, workspace, workspace_bytes, stream,
+                    softcap, alibi_slopes);
 }
 
 size_t attn_fwd_kvcache_workspace_bytes(int batch, int total_q, int max_seqlen_q, int nheads_q,

@@ -41,6 +41,7 @@ namespace {
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
 
 template <int D>
 struct FwdCfg {
@@ -389,7 +390,7 @@ __device__ __forceinline__ uint32_t sw128_unit(uint32_t base, int r, int u) {
     return base + (u >> 3) * (128 * 128) + r * 128 + (((u & 7) ^ (r & 7)) << 4);
 }
 
-template <int D, bool kPaged>
+template <int D, bool kPaged, bool kMods>
 __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32_t tmem,
                             const Watchdog& wd, int n_items, int t, int k, int lane) {
     using C = FwdCfg<D>;
@@ -414,7 +415,8 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
 #pragma unroll
     for (int c = 0; c < 4; ++c)
         st_addr[c] = p_tile + st_row * 128 + ((((2 * c + st_dc) ^ lane) & 7) << 4);
-    const float sl2 = p.scale_log2;
+    // log2(e) times what turns an S value into a logit (with modifiers S is made a logit first)
+    const float sl2 = kMods ? kLog2e : p.scale_log2;
     const uint64_t sl2x2 = f2_make(sl2, sl2);
     const int G = gridDim.x, cta = blockIdx.x;
     const int g = p.g;
@@ -431,6 +433,16 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
         if (!tv.rows) continue;
         // this thread's rows ra and ra + 8; packed row r is token tok0 + r / g, head kvh g + r % g
         float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;  // l: this thread's part
+        // ALiBi: the rows' slopes and bottom-right key positions
+        float slope_a = 0.f, slope_b = 0.f, pos_a = 0.f, pos_b = 0.f;
+        if constexpr (kMods) {
+            if (p.alibi != nullptr) {
+                slope_a = p.alibi[it.kvh * g + ra % g];
+                slope_b = p.alibi[it.kvh * g + (ra + 8) % g];
+                pos_a = static_cast<float>(tv.tok0 + ra / g + it.Lk - it.Lq);
+                pos_b = static_cast<float>(tv.tok0 + (ra + 8) / g + it.Lk - it.Lq);
+            }
+        }
         // Blocks needing the element mask are a prefix and a suffix of [lo, hi) (left window
         // edge; diagonal, right window edge, ragged end): the rest, [full_lo, full_hi), is
         // found once per item.
@@ -453,6 +465,36 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(s_free);
+                if constexpr (kMods) {
+                    // logits: scale, softcap c tanh(x / c) with tanh x = 1 - 2 / (e^(2x) + 1),
+                    // then the ALiBi bias; the element mask below comes after them
+                    if (p.softcap > 0.f) {
+                        const float k2 = 2.f * kLog2e * p.scale / p.softcap;
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) {
+                            const float y = ex2_approx(__uint_as_float(s[c]) * k2);
+                            s[c] = __float_as_uint(p.softcap * (1.f - 2.f * rcp_approx(1.f + y)));
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c)
+                            s[c] = __float_as_uint(__uint_as_float(s[c]) * p.scale);
+                    }
+                    if (p.alibi != nullptr) {
+                        const float key0 = static_cast<float>(j * kFwdBlockN + cpair);
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const float key = key0 + static_cast<float>(8 * c + e);
+                                s[4 * c + e] = __float_as_uint(
+                                    fmaf(-slope_a, fabsf(pos_a - key), __uint_as_float(s[4 * c + e])));
+                                s[4 * c + 2 + e] = __float_as_uint(
+                                    fmaf(-slope_b, fabsf(pos_b - key), __uint_as_float(s[4 * c + 2 + e])));
+                            }
+                        }
+                    }
+                }
                 if (j < full_lo || j >= full_hi) {
                     const int key0 = j * kFwdBlockN + cpair;
                     int kmin_a, kmax_a, kmin_b, kmax_b;
@@ -656,7 +698,7 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
     }
 }
 
-template <int D, bool kPaged>
+template <int D, bool kPaged, bool kMods>
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdParams p) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -713,7 +755,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         }
     } else {
         regs_increase<104>();
-        fwd_softmax<D, kPaged>(p, smem, bars, tmem, wd, n_items, warp >> 3, warp & 7, lane);
+        fwd_softmax<D, kPaged, kMods>(p, smem, bars, tmem, wd, n_items, warp >> 3, warp & 7, lane);
     }
     __syncwarp();
     tc_fence_before();
@@ -867,10 +909,12 @@ int fwd_smem_bytes(int head_dim) {
 
 cudaError_t configure_fwd_kernels() {
     const cudaFuncAttribute smem = cudaFuncAttributeMaxDynamicSharedMemorySize;
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<128, false>, smem, FwdCfg<128>::kSmem);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(fwd_kernel<64, false>, smem, FwdCfg<64>::kSmem);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(fwd_kernel<128, true>, smem, FwdCfg<128>::kSmem);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(fwd_kernel<64, true>, smem, FwdCfg<64>::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<128, false, false>, smem, FwdCfg<128>::kSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(fwd_kernel<64, false, false>, smem, FwdCfg<64>::kSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(fwd_kernel<128, true, false>, smem, FwdCfg<128>::kSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(fwd_kernel<64, true, false>, smem, FwdCfg<64>::kSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(fwd_kernel<128, false, true>, smem, FwdCfg<128>::kSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(fwd_kernel<64, false, true>, smem, FwdCfg<64>::kSmem);
     return e;
 }
 
@@ -879,19 +923,26 @@ cudaError_t launch_fwd_prepare(const FwdPrepParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-// K/V through block_table when p.block_table is set, else contiguous.
+// K/V through block_table when p.block_table is set, else contiguous; the score-modifier
+// instance when softcap or ALiBi is requested (contiguous K/V only).
 cudaError_t launch_fwd(const FwdParams& p, int head_dim, int grid, cudaStream_t stream) {
     const bool paged = p.block_table != nullptr;
+    const bool mods = p.softcap > 0.f || p.alibi != nullptr;
+    if (paged && mods) return cudaErrorInvalidValue;
     if (head_dim == 128) {
         if (paged)
-            fwd_kernel<128, true><<<grid, kFwdThreads, FwdCfg<128>::kSmem, stream>>>(p);
+            fwd_kernel<128, true, false><<<grid, kFwdThreads, FwdCfg<128>::kSmem, stream>>>(p);
+        else if (mods)
+            fwd_kernel<128, false, true><<<grid, kFwdThreads, FwdCfg<128>::kSmem, stream>>>(p);
         else
-            fwd_kernel<128, false><<<grid, kFwdThreads, FwdCfg<128>::kSmem, stream>>>(p);
+            fwd_kernel<128, false, false><<<grid, kFwdThreads, FwdCfg<128>::kSmem, stream>>>(p);
     } else {
         if (paged)
-            fwd_kernel<64, true><<<grid, kFwdThreads, FwdCfg<64>::kSmem, stream>>>(p);
+            fwd_kernel<64, true, false><<<grid, kFwdThreads, FwdCfg<64>::kSmem, stream>>>(p);
+        else if (mods)
+            fwd_kernel<64, false, true><<<grid, kFwdThreads, FwdCfg<64>::kSmem, stream>>>(p);
         else
-            fwd_kernel<64, false><<<grid, kFwdThreads, FwdCfg<64>::kSmem, stream>>>(p);
+            fwd_kernel<64, false, false><<<grid, kFwdThreads, FwdCfg<64>::kSmem, stream>>>(p);
     }
     return cudaGetLastError();
 }

@@ -56,6 +56,10 @@ struct FwdParams {
     int Hq, Hkv, g, tpt, total_q;
     int causal, wl, wr;
     float scale_log2;  // softmax_scale * log2(e)
+    // Score modifiers (the kernel instance built for them): softcap c > 0 maps the scaled
+    // score s to c tanh(s / c); alibi (per q head, or null) adds -slope |pos - key|.
+    float scale, softcap;
+    const float* alibi;
     // Paged K/V (block_table != null): tm_k / tm_v are 3-D over [num_pages * page_size, Hkv, d]
     // with boxes {64, 1, box_rows}; sequence b holds cache_seqlens[b] + q_len_b keys.
     const int* block_table;     // [batch, max_pages]

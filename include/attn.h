@@ -223,6 +223,23 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
 /* Workspace bytes for attn_bwd (D, fp32 per (head, token)). */
 size_t attn_bwd_workspace_bytes(int total_q, int nheads_q);
 
+/*
+ * attn_fwd with the score modifiers of "04 · FA4 (CuTeDSL) and engineering interfaces",
+ * section 7, applied to each scaled score s = softmax_scale * q.k before the mask:
+ *   softcap > 0     s -> softcap * tanh(s / softcap)      (0 = off)
+ *   alibi_slopes    device fp32 [nheads_q] or NULL: s -> s - slope_h * |i + Lk - Lq - j|
+ *                   (query i at its bottom-right position, key j)
+ * LSE is that of the modified scores.  Other arguments, layouts and errors as attn_fwd;
+ * softcap must be finite and >= 0.
+ */
+attn_status_t attn_fwd_mods(const void* q, const void* k, const void* v, void* out, float* lse,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch,
+                            int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                            int nheads_q, int nheads_kv, int head_dim, float softmax_scale,
+                            int causal, int window_left, int window_right, float softcap,
+                            const float* alibi_slopes, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
 /* Bytes of split-partial workspace for attn_decode_kvcache; num_splits 0 sizes for the
  * automatic choice (at most 16 splits).  0 when one split needs no workspace. */
 size_t attn_decode_workspace_bytes(int batch, int nheads_q, int head_dim, int num_splits);

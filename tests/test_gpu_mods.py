@@ -1,0 +1,54 @@
+"""Score modifiers (attn_fwd_mods: softcap, ALiBi) versus the fp64 oracle, full rows, with
+the parity tolerances of the plain forward pass."""
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_70_gb300 import synth
+from oracle import oracle
+from tests.parity import compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def attn():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from exact_attention_70_gb300 import build as attn_build
+    attn_build.build()
+    from exact_attention_70_gb300 import binding
+    binding.load()
+    return binding
+
+
+CASES = [
+    # (lengths_q, lengths_k, Hq, Hkv, d, causal, window, softcap, alibi)
+    ([300, 77], None, 4, 2, 128, True, (-1, -1), 30.0, False),
+    ([300, 77], None, 4, 2, 128, True, (-1, -1), 0.0, True),
+    ([500], None, 8, 2, 128, True, (-1, -1), 5.0, True),
+    ([200, 129], None, 4, 4, 64, False, (-1, -1), 2.0, True),
+    ([400], [600], 4, 1, 128, True, (100, 0), 20.0, True),   # bottom-right, window
+    ([260], None, 6, 2, 128, False, (40, 40), 0.0, True),    # g = 3
+]
+
+
+@pytest.mark.parametrize("idx", range(len(CASES)))
+def test_modifiers_match_oracle(attn, idx):
+    lq, lk, Hq, Hkv, d, causal, window, cap, alibi = CASES[idx]
+    c = synth.prefill_case(lq, Hq, Hkv, d, causal, seed=800 + idx, lengths_k=lk, window=window,
+                           name=f"mods{idx}")
+    slopes = torch.tensor([2.0 ** (-8.0 * (h + 1) / Hq) for h in range(Hq)], dtype=torch.float32) \
+        if alibi else None
+    dev = "cuda"
+    out, lse = attn.attn_fwd_mods(c.q.to(dev), c.k.to(dev), c.v.to(dev), c.cu_seqlens_q.to(dev),
+                                  c.cu_seqlens_k.to(dev), c.max_seqlen_q, c.max_seqlen_k,
+                                  c.softmax_scale, c.causal, c.window_left, c.window_right,
+                                  softcap=cap, alibi_slopes=slopes.to(dev) if alibi else None)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == 0
+    o_ref, l_ref = oracle.attn_fwd_mods(c.q, c.k, c.v, c.cu_seqlens_q, c.cu_seqlens_k,
+                                        c.softmax_scale, c.causal, c.window_left, c.window_right,
+                                        softcap=cap,
+                                        alibi_slopes=slopes.double().numpy() if alibi else None)
+    compare(out.cpu(), lse.cpu().T, o_ref, l_ref.T, c.name)

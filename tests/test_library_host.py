@@ -206,3 +206,20 @@ def test_bwd_arguments_are_rejected_before_any_launch(lib):
     assert call(11, 0) == 0        # batch 0
     assert lib.attn_bwd_workspace_bytes(1000, 8) == (32000 + 255) // 256 * 256
     assert lib.attn_bwd_workspace_bytes(1001, 8) == (32032 + 255) // 256 * 256
+
+
+def test_modifier_arguments_are_checked(lib):
+    P = ctypes.c_void_p
+    fake = P(4096)
+    f = lib.attn_fwd_mods
+    base = [fake] * 7 + [1, 16, 16, 16, 16, 4, 2, 128, 0.1, 1, -1, -1, 0.0, None, fake, 1 << 20, None]
+
+    def call(i, v):
+        a = list(base)
+        a[i] = v
+        return f(*a)
+
+    assert call(19, -1.0) == -1              # negative softcap
+    assert call(19, float("nan")) == -1
+    assert call(20, P(4098)) == -1           # misaligned slopes
+    assert call(7, 0) == 0                   # batch 0
