@@ -10,15 +10,18 @@
 // GB300 mapping: three kernels, no atomics (dQ is accumulated in one CTA, so the result does
 // not depend on scheduling):
 //   * bwd_preprocess_kernel: D per (token, head), one warp per row;
-//   * bwd_dkdv_kernel: one CTA per 128-key block of one (sequence, kv head); it walks the
-//     128-row Q tiles (tokens x the g query heads, packed as in the forward pass) that see
-//     the block, with S^T = K Q^T and dP^T = V dO^T in TMEM, P^T and dS^T written back over
-//     them as bf16, and dV += P^T dO, dK += dS^T Q accumulated in TMEM;
-//   * bwd_dq_kernel: one CTA per Q tile, walking the key blocks it sees, with S, dP in TMEM,
-//     dS written back over S as bf16 and dQ += dS K accumulated in TMEM.
-//   Roles per CTA: warps 0-7 the elementwise work (two warps per TMEM lane quarter, each
-//   taking half of the columns), warp 8 TMA, warp 9 the MMA issuer and TMEM owner.
+//   * bwd_dkdv_kernel: one CTA per 128-key block of one (sequence, kv head), walking the
+//     128-row Q tiles (tokens x query heads, packed as in the forward pass) that see it;
+//   * bwd_dq_kernel: one CTA per 128-row Q tile, walking the 128-key blocks it sees.
+//   Every MMA is 128 x 128 (x D) so the tensor pipe runs at its full rate.  The elementwise
+//   warps (0-7, two per TMEM lane quarter) pull S and dP of a block into registers first, which
+//   frees the TMEM region for the next block's MMA while they work; the gradient operand goes
+//   back as bf16 over dP^T in TMEM (dK/dV kernel) or to a 128-byte-swizzled shared-memory slot
+//   (dQ kernel).  Warp 9 issues the MMAs, warp 8 streams operands by TMA, and in the dK/dV
+//   kernel warps 10-11 stage the query rows' L, D and key intervals a tile ahead.
 #include <cuda_bf16.h>
+
+#include <cstddef>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -30,23 +33,47 @@ namespace {
 
 constexpr float kLog2e = 1.44269504088896341f;
 constexpr int kBwdThreads = 384;
+constexpr int kStages = 2;  // streamed operand ring (and row information ring)
 
 template <int D>
 struct BwdCfg {
-    static constexpr int kHalves = D / 64;
-    static constexpr int kAtomBytes = 128 * 128;
-    static constexpr int kTile = kHalves * kAtomBytes;  // 128 rows x D bf16, 128-B swizzle
+    static constexpr int kHalves = D / 64;      // 128-byte swizzle atoms across d
+    static constexpr int kAtom = 128 * 128;     // one atom of 128 rows x 128 bytes
+    static constexpr int kTile = kHalves * kAtom;
 };
 
 struct BwdBars {
-    uint64_t kv_full[2], kv_empty[2], q_full[2], q_empty[2];
-    uint64_t s_full, p_full, mm_done, drain;
+    uint64_t fixed_full;                               // loaded once (dK/dV: K, V; dQ: Q, dO)
+    uint64_t in_full[kStages], in_empty[kStages];      // streamed operands
+    uint64_t info_full[kStages], info_empty[kStages];  // row information (dK/dV)
+    uint64_t s_full, s_free;                           // S / dP in TMEM, loaded to registers
+    uint64_t p_full[2], p_empty;                       // P^T, dS^T (TMEM) or dS (shared)
+    uint64_t g_done, mm_done, drain;
     uint32_t tmem_base;
     int abort_flag;
 };
 
-// Per packed row of a Q tile: -L * log2(e) (or -inf when the row has no gradient), D, and
-// the row's visible key interval.
+__device__ void init_bars(BwdBars* b) {
+    mbar_init(&b->fixed_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+        mbar_init(&b->in_full[s], 1);
+        mbar_init(&b->in_empty[s], 1);
+        mbar_init(&b->info_full[s], 64);
+        mbar_init(&b->info_empty[s], 8);
+    }
+    mbar_init(&b->s_full, 1);
+    mbar_init(&b->s_free, 8);
+    mbar_init(&b->p_full[0], 8);
+    mbar_init(&b->p_full[1], 8);
+    mbar_init(&b->p_empty, 1);
+    mbar_init(&b->g_done, 1);
+    mbar_init(&b->mm_done, 1);
+    mbar_init(&b->drain, 1);
+    b->abort_flag = 0;
+}
+
+// Per packed row of a 128-row Q tile: -L * log2(e) (or -inf when the row has no gradient),
+// D, and the row's visible key interval.
 struct RowInfo {
     float nl[128];
     float dd[128];
@@ -58,6 +85,34 @@ __device__ void bwd_drain(uint64_t* bar, uint32_t parity) {
     const unsigned long long t0 = global_ns();
     while (!mbar_try(bar, parity))
         if (global_ns() - t0 > 200000000ull) return;
+}
+
+// 32 fp32 accumulator columns times mul, as bf16, to 64 contiguous bytes of global memory.
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&o)[32], float mul) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+        d4[v] = make_uint4(
+            pack_bf16x2(__uint_as_float(o[8 * v + 0]) * mul, __uint_as_float(o[8 * v + 1]) * mul),
+            pack_bf16x2(__uint_as_float(o[8 * v + 2]) * mul, __uint_as_float(o[8 * v + 3]) * mul),
+            pack_bf16x2(__uint_as_float(o[8 * v + 4]) * mul, __uint_as_float(o[8 * v + 5]) * mul),
+            pack_bf16x2(__uint_as_float(o[8 * v + 6]) * mul, __uint_as_float(o[8 * v + 7]) * mul));
+}
+
+// P = exp2(s * scale_log2 + nl) and dS = P (dp - dd) for two elements, with the paired fp32
+// instructions (two lanes of work per issue); a masked element gets P = 0.
+__device__ __forceinline__ void p_ds_pair(uint32_t s0, uint32_t s1, uint32_t dp0, uint32_t dp1,
+                                          uint64_t scale2, uint64_t nl2, uint64_t ndd2, bool m0,
+                                          bool m1, uint32_t& p_out, uint32_t& ds_out) {
+    float x0, x1;
+    f2_split(f2_fma(f2_make(__uint_as_float(s0), __uint_as_float(s1)), scale2, nl2), x0, x1);
+    const float p0 = ex2_approx(m0 ? -INFINITY : x0);
+    const float p1 = ex2_approx(m1 ? -INFINITY : x1);
+    const uint64_t pv = f2_make(p0, p1);
+    float d0, d1;
+    f2_split(f2_mul(pv, f2_add(f2_make(__uint_as_float(dp0), __uint_as_float(dp1)), ndd2)), d0, d1);
+    p_out = pack_bf16x2(p0, p1);
+    ds_out = pack_bf16x2(d0, d1);
 }
 
 // The sequence of (b, kvh) a CTA serves, checked against the tensors.
@@ -77,28 +132,6 @@ __device__ __forceinline__ BwdSeq bwd_seq(const BwdParams& p) {
     s.ok = s.q0 >= 0 && s.Lq >= 0 && s.q0 + s.Lq <= p.total_q && s.Lq <= p.max_seqlen_q &&
            s.k0 >= 0 && s.Lk >= 0 && s.k0 + s.Lk <= p.total_k && s.Lk <= p.max_seqlen_k;
     return s;
-}
-
-// Fill row information of Q tile i for packed rows r = 0..127 (threads 0..127 of the warps
-// 0-7).  Rows past the tile's tokens or the sequence get no gradient (nl = -inf, D = 0).
-__device__ void fill_rows(const BwdParams& p, const BwdSeq& sq, int i, bool masked, RowInfo& ri,
-                          int r) {
-    const int tok = i * p.tpt + r / p.g;
-    const int head = sq.kvh * p.g + r % p.g;
-    const bool valid = r < p.g * p.tpt && tok < sq.Lq;
-    float nl = -INFINITY, dd = 0.f;
-    int kmin = 1, kmax = 0;
-    if (valid) {
-        const size_t at = static_cast<size_t>(head) * p.total_q + sq.q0 + tok;
-        const float l = p.lse[at];
-        if (l != -INFINITY) nl = -l * kLog2e;
-        dd = p.dsum[at];
-        if (masked) row_key_interval(tok, sq.Lq, sq.Lk, p.causal, p.wl, p.wr, kmin, kmax);
-    }
-    ri.nl[r] = nl;
-    ri.dd[r] = dd;
-    ri.kmin[r] = kmin;
-    ri.kmax[r] = kmax;
 }
 
 // ---- D = rowsum(dO * O) ---------------------------------------------------------------------
@@ -127,19 +160,45 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
 }
 
 // ---- dK, dV: one CTA per key block --------------------------------------------------------
+//
+// The CTA walks the 128-row Q tiles that see key block j.  TMEM: S^T at [0, 128), dP^T at
+// [128, 256), dV at [256, 256 + D), dK at [256 + D, 256 + 2 D).  Tile n:
+//   warps 0-7:   load their 64 columns of S^T(n) to registers (the S^T region is free again),
+//                then per 32-column chunk load dP^T, form P^T = exp2(S^T scale log2(e) -
+//                L log2(e)) and dS^T = P^T (dP^T - D), and write both as packed bf16 over the
+//                chunk's own dP^T columns (P^T in the first 16, dS^T in the last 16);
+//   MMA warp:    S^T(n+1) = K Q(n+1)^T as soon as S^T(n) is in registers; dV += P^T dO and
+//                dK += dS^T Q (A from TMEM) in two halves as the chunks arrive; dP^T(n+1) =
+//                V dO(n+1)^T once those have read the dP^T region;
+//   warps 10-11: the rows' -L log2(e), D and key intervals, a tile ahead;
+//   warp 8:      TMA of K, V (once) and of Q, dO tiles (two stages).
+
+template <int D>
+struct DkdvSmem {
+    using C = BwdCfg<D>;
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = C::kTile;
+    static constexpr int kOffQ = 2 * C::kTile;                 // kStages stages
+    static constexpr int kOffDO = kOffQ + kStages * C::kTile;   // kStages stages
+    static constexpr int kOffInfo = kOffDO + kStages * C::kTile;
+    static constexpr int kOffBars = kOffInfo + kStages * static_cast<int>(sizeof(RowInfo));
+    static constexpr int kBytes = kOffBars + static_cast<int>(sizeof(BwdBars)) + 1024;
+};
+static_assert(DkdvSmem<128>::kBytes <= 227 * 1024, "dK/dV shared memory");
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using C = BwdCfg<D>;
+    using L = DkdvSmem<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* sK = smem;
-    uint8_t* sV = smem + C::kTile;
-    uint8_t* sQ = smem + 2 * C::kTile;   // two stages
-    uint8_t* sDO = smem + 4 * C::kTile;  // two stages
-    RowInfo* info = reinterpret_cast<RowInfo*>(smem + 6 * C::kTile);  // two stages
-    BwdBars* bars = reinterpret_cast<BwdBars*>(smem + 6 * C::kTile + 2 * sizeof(RowInfo));
+    uint8_t* sK = smem + L::kOffK;
+    uint8_t* sV = smem + L::kOffV;
+    uint8_t* sQ = smem + L::kOffQ;
+    uint8_t* sDO = smem + L::kOffDO;
+    RowInfo* info = reinterpret_cast<RowInfo*>(smem + L::kOffInfo);
+    BwdBars* bars = reinterpret_cast<BwdBars*>(smem + L::kOffBars);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const BwdSeq sq = bwd_seq(p);
@@ -150,30 +209,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     const int j = blockIdx.x;  // key block
     if (j * 128 >= sq.Lk) return;
     const int n_qt = (sq.Lq + p.tpt - 1) / p.tpt;
+    auto tok_hi = [&](int i) { return min(i * p.tpt + p.tpt, sq.Lq) - 1; };
     // Does Q tile i see key block j?  (the forward pass's block range, per tile)
     auto sees = [&](int i) {
-        const KvRange r = kv_block_range(i * p.tpt, min(i * p.tpt + p.tpt, sq.Lq) - 1, sq.Lq,
-                                         sq.Lk, 128, p.causal, p.wl, p.wr);
+        const KvRange r = kv_block_range(i * p.tpt, tok_hi(i), sq.Lq, sq.Lk, 128, p.causal, p.wl,
+                                         p.wr);
         return r.lo <= j && j < r.hi;
     };
 
     // Rows of Q and dO past the packed tokens are never written by TMA but are part of the
     // contractions over query rows: clear both stages once.
-    for (int u = threadIdx.x; u < 4 * C::kTile / 16; u += blockDim.x)
+    for (int u = threadIdx.x; u < 2 * kStages * C::kTile / 16; u += blockDim.x)
         st_shared_v4(smem_u32(sQ) + u * 16, 0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
     if (threadIdx.x == 0) {
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars->kv_full[s], 1);
-            mbar_init(&bars->kv_empty[s], 1);
-            mbar_init(&bars->q_full[s], 1);
-            mbar_init(&bars->q_empty[s], 1);
-        }
-        mbar_init(&bars->s_full, 1);
-        mbar_init(&bars->p_full, 8);
-        mbar_init(&bars->mm_done, 1);
-        mbar_init(&bars->drain, 1);
-        bars->abort_flag = 0;
+        init_bars(bars);
         mbar_fence_init();
     }
     if (warp == 9) tmem_alloc(&bars->tmem_base, 512);
@@ -182,44 +232,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     const Watchdog wd{&bars->abort_flag, p.status};
-    // TMEM: S^T / P^T [0, 128), dP^T / dS^T [128, 256), dV [256, 256 + D), dK [256 + D, ...)
-    constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+    constexpr uint32_t kColS = 0, kColG = 128, kColDV = 256, kColDK = 256 + D;
 
-    // Registers: launched at 168 per thread; warpgroup 2 (TMA, MMA, two idle warps) drops to
-    // 80 and the elementwise warps rise to 208: 128 * 80 + 256 * 208 = 63488 <= 384 * 168.
-    // (Each role sets its own count inside its branch.)
+    // Registers: launched at 168 per thread; warps 8-11 drop to 80 and the elementwise warps
+    // rise to 208: 128 * 80 + 256 * 208 = 63488 <= 384 * 168.  (Each role sets its own count.)
     if (warp == 8) {
         regs_decrease<80>();
         if (lane == 0) {
             tma_prefetch_desc(&p.tm_q);
             tma_prefetch_desc(&p.tm_do);
-            mbar_arrive_expect_tx(&bars->kv_full[0], 2 * C::kTile);
+            mbar_arrive_expect_tx(&bars->fixed_full, 2 * C::kTile);
 #pragma unroll
             for (int h = 0; h < C::kHalves; ++h) {
-                tma_load_3d(sK + h * C::kAtomBytes, &p.tm_k, &bars->kv_full[0], h * 64, sq.kvh,
+                tma_load_3d(sK + h * C::kAtom, &p.tm_k, &bars->fixed_full, h * 64, sq.kvh,
                             sq.k0 + j * 128);
-                tma_load_3d(sV + h * C::kAtomBytes, &p.tm_v, &bars->kv_full[0], h * 64, sq.kvh,
+                tma_load_3d(sV + h * C::kAtom, &p.tm_v, &bars->fixed_full, h * 64, sq.kvh,
                             sq.k0 + j * 128);
             }
-            const uint32_t box = 64u * p.g * p.tpt * 2u * C::kHalves;
-            uint32_t n = 0;
+            const uint32_t box = 128u * p.g * p.tpt * C::kHalves;  // bytes of one operand
+            int n = 0;
             for (int i = 0; i < n_qt; ++i) {
                 if (!sees(i)) continue;
-                const int s = n & 1;
-                if (n >= 2 && !wd.wait(&bars->q_empty[s], ((n >> 1) - 1) & 1)) break;
-                mbar_arrive_expect_tx(&bars->q_full[s], 2 * box);
+                const int st = n & 1;
+                if (n >= 2 && !wd.wait(&bars->in_empty[st], ((n >> 1) - 1) & 1)) break;
+                mbar_arrive_expect_tx(&bars->in_full[st], 2 * box);
 #pragma unroll
                 for (int h = 0; h < C::kHalves; ++h) {
-                    tma_load_3d(sQ + s * C::kTile + h * C::kAtomBytes, &p.tm_q, &bars->q_full[s],
+                    tma_load_3d(sQ + st * C::kTile + h * C::kAtom, &p.tm_q, &bars->in_full[st],
                                 h * 64, sq.kvh * p.g, sq.q0 + i * p.tpt);
-                    tma_load_3d(sDO + s * C::kTile + h * C::kAtomBytes, &p.tm_do,
-                                &bars->q_full[s], h * 64, sq.kvh * p.g, sq.q0 + i * p.tpt);
+                    tma_load_3d(sDO + st * C::kTile + h * C::kAtom, &p.tm_do, &bars->in_full[st],
+                                h * 64, sq.kvh * p.g, sq.q0 + i * p.tpt);
                 }
                 ++n;
             }
-            bwd_drain(&bars->kv_full[0], 0);
-            for (uint32_t s = 0; s < 2 && s < n; ++s)
-                bwd_drain(&bars->q_full[s], ((n - 1 - s) >> 1) & 1);
+            bwd_drain(&bars->fixed_full, 0);
+            for (int m = n > 2 ? n - 2 : 0; m < n; ++m) bwd_drain(&bars->in_full[m & 1], (m >> 1) & 1);
         }
     } else if (warp == 9) {
         regs_decrease<80>();
@@ -228,105 +275,170 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             constexpr uint32_t kIdG = idesc_bf16_f32(128, D, false, true);
             const uint64_t dk_ = sdesc_sw128(smem_u32(sK), 16, 1024);
             const uint64_t dv_ = sdesc_sw128(smem_u32(sV), 16, 1024);
-            uint32_t n = 0;
-            if (wd.wait(&bars->kv_full[0], 0)) {
-                for (int i = 0; i < n_qt; ++i) {
-                    if (!sees(i)) continue;
-                    const int s = n & 1;
-                    if (!wd.wait(&bars->q_full[s], (n >> 1) & 1)) break;
-                    // S^T and dP^T overwrite P^T and dS^T of the previous tile
-                    if (n > 0 && !wd.wait(&bars->mm_done, (n - 1) & 1)) break;
-                    tc_fence_after();
-                    const uint32_t q_base = smem_u32(sQ + s * C::kTile);
-                    const uint32_t do_base = smem_u32(sDO + s * C::kTile);
-                    const uint64_t dq_ = sdesc_sw128(q_base, 16, 1024);
-                    const uint64_t ddo = sdesc_sw128(do_base, 16, 1024);
+            // X^T = A B^T over d into TMEM column col, B a Q / dO stage
+            auto s_mma = [&](uint32_t col, uint64_t a, const uint8_t* b) {
+                const uint64_t bd = sdesc_sw128(smem_u32(b), 16, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t off = (((kk >> 2) * C::kAtomBytes + (kk & 3) * 32) >> 4);
-                        umma_ss(tmem + kColS, dk_ + off, dq_ + off, kIdS, kk > 0);
-                        umma_ss(tmem + kColDP, dv_ + off, ddo + off, kIdS, kk > 0);
-                    }
-                    umma_commit(&bars->s_full);
-                    if (!wd.wait(&bars->p_full, n & 1)) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < 128 / 16; ++kk) {
-                        const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
-                        umma_ts(tmem + kColDV, tmem + kColS + kk * 8,
-                                sdesc_sw128(do_base + kk * 2048, C::kAtomBytes, 1024), kIdG, acc);
-                        umma_ts(tmem + kColDK, tmem + kColDP + kk * 8,
-                                sdesc_sw128(q_base + kk * 2048, C::kAtomBytes, 1024), kIdG, acc);
-                    }
-                    umma_commit(&bars->mm_done);
-                    umma_commit(&bars->q_empty[s]);
-                    ++n;
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = (((kk >> 2) * C::kAtom + (kk & 3) * 32) >> 4);
+                    umma_ss(tmem + col, a + off, bd + off, kIdS, kk > 0);
                 }
+            };
+            // dV += P^T dO, dK += dS^T Q of tile m (stage st), K-steps of query rows 16 kk:
+            // half h holds the steps kk with (kk >> 1) & 1 == h, written by the chunk c2 == h
+            // of both column halves
+            auto grads = [&](int m, int st) {
+                const uint32_t q_base = smem_u32(sQ + st * C::kTile);
+                const uint32_t do_base = smem_u32(sDO + st * C::kTile);
+                for (int h = 0; h < 2; ++h) {
+                    if (!wd.wait(&bars->p_full[h], m & 1)) return false;
+                    tc_fence_after();
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int kk = 4 * (u >> 1) + 2 * h + (u & 1);
+                        const uint32_t a_col = kColG + 32 * (kk >> 1) + 8 * (kk & 1);
+                        const uint32_t acc = (m > 0 || u > 0 || h > 0) ? 1u : 0u;
+                        umma_ts(tmem + kColDV, tmem + a_col,
+                                sdesc_sw128(do_base + kk * 2048, C::kAtom, 1024), kIdG, acc);
+                        umma_ts(tmem + kColDK, tmem + a_col + 16,
+                                sdesc_sw128(q_base + kk * 2048, C::kAtom, 1024), kIdG, acc);
+                    }
+                }
+                umma_commit(&bars->g_done);
+                umma_commit(&bars->in_empty[st]);
+                return true;
+            };
+            int n = 0, prev_st = 0;
+            bool ok = wd.wait(&bars->fixed_full, 0);
+            for (int i = 0; ok && i < n_qt; ++i) {
+                if (!sees(i)) continue;
+                const int st = n & 1;
+                ok = wd.wait(&bars->in_full[st], (n >> 1) & 1);
+                // S^T(n) over S^T(n-1), which the elementwise warps have in registers
+                if (ok && n >= 1) ok = wd.wait(&bars->s_free, (n - 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                s_mma(kColS, dk_, sQ + st * C::kTile);
+                // dP^T(n) over P^T, dS^T of tile n - 1 once dV, dK have read them
+                if (n >= 1) {
+                    ok = grads(n - 1, prev_st) && wd.wait(&bars->g_done, (n - 1) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                s_mma(kColG, dv_, sDO + st * C::kTile);
+                umma_commit(&bars->s_full);
+                prev_st = st;
+                ++n;
             }
+            if (ok && n >= 1) grads(n - 1, prev_st);
+            umma_commit(&bars->mm_done);
             umma_commit(&bars->drain);
             bwd_drain(&bars->drain, 0);
         }
     } else if (warp >= 10) {
         regs_decrease<80>();
+        // Row information of each tile: thread r fills packed rows r and r + 64.
+        const int r0 = threadIdx.x - 320;
+        int n = 0;
+        for (int i = 0; i < n_qt; ++i) {
+            if (!sees(i)) continue;
+            const int st = n & 1;
+            if (n >= 2 && !wd.wait(&bars->info_empty[st], ((n >> 1) - 1) & 1)) break;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = r0 + 64 * h;
+                const int tok = i * p.tpt + r / p.g;
+                float nl = -INFINITY, dd = 0.f;
+                int kmin = 1, kmax = 0;
+                if (r < p.g * p.tpt && tok < sq.Lq) {
+                    const size_t at =
+                        static_cast<size_t>(sq.kvh * p.g + r % p.g) * p.total_q + sq.q0 + tok;
+                    const float l = p.lse[at];
+                    if (l != -INFINITY) nl = -l * kLog2e;
+                    dd = p.dsum[at];
+                    row_key_interval(tok, sq.Lq, sq.Lk, p.causal, p.wl, p.wr, kmin, kmax);
+                }
+                info[st].nl[r] = nl;
+                info[st].dd[r] = -dd;
+                info[st].kmin[r] = kmin;
+                info[st].kmax[r] = kmax;
+            }
+            mbar_arrive(&bars->info_full[st]);
+            ++n;
+        }
     } else {
         regs_increase<208>();
         const int quarter = warp & 3, ch = warp >> 2;
         const int kr = 32 * quarter + lane;  // key row of the block
         const int key = j * 128 + kr;
         const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
-        // Every compute warp passes both named barriers on every tile, even after a wait has
-        // run out (ok == false skips the work), so no warp is left waiting at one.
+        const uint64_t scale2 = f2_make(p.scale_log2, p.scale_log2);
         bool ok = true;
-        uint32_t n = 0;
+        int n = 0;
         for (int i = 0; i < n_qt; ++i) {
             if (!sees(i)) continue;
-            const int s = n & 1;
-            const int imin = i * p.tpt, imax = min(imin + p.tpt, sq.Lq) - 1;
-            const bool masked = kv_block_masked(j, imin, imax, sq.Lq, sq.Lk, 128, p.causal, p.wl,
-                                                p.wr);
-            if (threadIdx.x < 128) fill_rows(p, sq, i, masked, info[s], threadIdx.x);
-            named_bar_sync(1, 256);
+            const int st = n & 1;
+            const bool masked = kv_block_masked(j, i * p.tpt, tok_hi(i), sq.Lq, sq.Lk, 128,
+                                                p.causal, p.wl, p.wr);
             ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->s_full, n & 1));
             tc_fence_after();
-            const RowInfo& ri = info[s];
-            uint32_t pp[32], pd[32];
-#pragma unroll
-            for (int c2 = 0; c2 < 2 && ok; ++c2) {
-                const int col0 = 64 * ch + 32 * c2;
-                uint32_t sv[32], dv[32];
-                tmem_ld32(tmem + lane_off + kColS + col0, sv);
-                tmem_ld32(tmem + lane_off + kColDP + col0, dv);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float pe[2], de[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int c = col0 + e + u;
-                        float x = fmaf(__uint_as_float(sv[e + u]), p.scale_log2, ri.nl[c]);
-                        if (masked && (key < ri.kmin[c] || key > ri.kmax[c])) x = -INFINITY;
-                        pe[u] = ex2_approx(x);
-                        de[u] = pe[u] * (__uint_as_float(dv[e + u]) - ri.dd[c]);
-                    }
-                    pp[16 * c2 + e / 2] = pack_bf16x2(pe[0], pe[1]);
-                    pd[16 * c2 + e / 2] = pack_bf16x2(de[0], de[1]);
-                }
-            }
-            // every warp has read S^T and dP^T before any overwrites them with P^T and dS^T
-            named_bar_sync(2, 256);
+            uint32_t sv[64];
             if (ok) {
-                tmem_st32(tmem + lane_off + kColS + 32 * ch, pp);
-                tmem_st32(tmem + lane_off + kColDP + 32 * ch, pd);
-                tmem_wait_st();
+                tmem_ld32(tmem + lane_off + kColS + 64 * ch, *reinterpret_cast<uint32_t(*)[32]>(sv));
+                tmem_ld32(tmem + lane_off + kColS + 64 * ch + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+                tmem_wait_ld();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->s_free);
+            ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->info_full[st], (n >> 1) & 1));
+            const uint32_t ib = smem_u32(&info[st]);
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+                const uint32_t col = kColG + 64 * ch + 32 * c2;
+                if (ok) {
+                    uint32_t dv[32], pp[16], pd[16];
+                    tmem_ld32(tmem + lane_off + col, dv);
+                    tmem_wait_ld();
+                    const uint32_t ibc = ib + 4 * (64 * ch + 32 * c2);
+#pragma unroll
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const uint4 nl4 = ld_shared_v4(ibc + offsetof(RowInfo, nl) + 16 * e4);
+                        const uint4 dd4 = ld_shared_v4(ibc + offsetof(RowInfo, dd) + 16 * e4);
+                        bool m[4] = {false, false, false, false};
+                        if (masked) {
+                            const uint4 lo4 = ld_shared_v4(ibc + offsetof(RowInfo, kmin) + 16 * e4);
+                            const uint4 hi4 = ld_shared_v4(ibc + offsetof(RowInfo, kmax) + 16 * e4);
+                            m[0] = key < static_cast<int>(lo4.x) || key > static_cast<int>(hi4.x);
+                            m[1] = key < static_cast<int>(lo4.y) || key > static_cast<int>(hi4.y);
+                            m[2] = key < static_cast<int>(lo4.z) || key > static_cast<int>(hi4.z);
+                            m[3] = key < static_cast<int>(lo4.w) || key > static_cast<int>(hi4.w);
+                        }
+                        const int e = 32 * c2 + 4 * e4;
+                        p_ds_pair(sv[e], sv[e + 1], dv[4 * e4], dv[4 * e4 + 1], scale2,
+                                  f2_make(__uint_as_float(nl4.x), __uint_as_float(nl4.y)),
+                                  f2_make(__uint_as_float(dd4.x), __uint_as_float(dd4.y)), m[0],
+                                  m[1], pp[2 * e4], pd[2 * e4]);
+                        p_ds_pair(sv[e + 2], sv[e + 3], dv[4 * e4 + 2], dv[4 * e4 + 3], scale2,
+                                  f2_make(__uint_as_float(nl4.z), __uint_as_float(nl4.w)),
+                                  f2_make(__uint_as_float(dd4.z), __uint_as_float(dd4.w)), m[2],
+                                  m[3], pp[2 * e4 + 1], pd[2 * e4 + 1]);
+                    }
+                    tmem_st16(tmem + lane_off + col, pp);
+                    tmem_st16(tmem + lane_off + col + 16, pd);
+                    tmem_wait_st();
+                }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->p_full);
+                if (lane == 0) mbar_arrive(&bars->p_full[c2]);
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->info_empty[st]);
             ++n;
         }
         // Epilogue: dV and scale * dK rows of this key block, bf16.
         if (n > 0) {
-            ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->mm_done, (n - 1) & 1));
+            ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->mm_done, 0));
             tc_fence_after();
         }
         const bool valid = ok && key < sq.Lk;
@@ -346,16 +458,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = 0u;
                 }
-                if (valid) {
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        d4[v] = make_uint4(
-                            pack_bf16x2(__uint_as_float(o[8 * v + 0]) * mul, __uint_as_float(o[8 * v + 1]) * mul),
-                            pack_bf16x2(__uint_as_float(o[8 * v + 2]) * mul, __uint_as_float(o[8 * v + 3]) * mul),
-                            pack_bf16x2(__uint_as_float(o[8 * v + 4]) * mul, __uint_as_float(o[8 * v + 5]) * mul),
-                            pack_bf16x2(__uint_as_float(o[8 * v + 6]) * mul, __uint_as_float(o[8 * v + 7]) * mul));
-                }
+                if (valid) store_row32(dst + 32 * c, o, mul);
             }
         }
     }
@@ -369,19 +472,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
 }
 
 // ---- dQ: one CTA per Q tile ---------------------------------------------------------------
+//
+// The CTA walks the 128-key blocks its 128 packed query rows see.  TMEM: S at [0, 128), dP at
+// [128, 256), dQ at [256, 256 + D).  Block n:
+//   warps 0-7:  load their 64 columns of S(n) and dP(n) to registers (both regions are free
+//               again), form dS = P (dP - D) and write it as bf16 to the shared-memory slot;
+//   MMA warp:   S(n+1) = Q K(n+1)^T and dP(n+1) = dO V(n+1)^T as soon as S(n), dP(n) are in
+//               registers, then dQ += dS(n) K(n) with both operands in shared memory;
+//   warp 8:     TMA of Q, dO (once) and of K, V blocks (two stages).
+
+template <int D>
+struct DqSmem {
+    using C = BwdCfg<D>;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffDO = C::kTile;
+    static constexpr int kOffK = 2 * C::kTile;                // kStages stages
+    static constexpr int kOffV = kOffK + kStages * C::kTile;   // kStages stages
+    static constexpr int kOffDS = kOffV + kStages * C::kTile;  // 128 rows x 128 keys bf16
+    static constexpr int kOffBars = kOffDS + 2 * C::kAtom;
+    static constexpr int kBytes = kOffBars + static_cast<int>(sizeof(BwdBars)) + 1024;
+};
+static_assert(DqSmem<128>::kBytes <= 227 * 1024, "dQ shared memory");
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using C = BwdCfg<D>;
+    using L = DqSmem<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* sQ = smem;
-    uint8_t* sDO = smem + C::kTile;
-    uint8_t* sK = smem + 2 * C::kTile;  // two stages
-    uint8_t* sV = smem + 4 * C::kTile;  // two stages
-    RowInfo* info = reinterpret_cast<RowInfo*>(smem + 6 * C::kTile);
-    BwdBars* bars = reinterpret_cast<BwdBars*>(smem + 6 * C::kTile + 2 * sizeof(RowInfo));
+    uint8_t* sQ = smem + L::kOffQ;
+    uint8_t* sDO = smem + L::kOffDO;
+    uint8_t* sK = smem + L::kOffK;
+    uint8_t* sV = smem + L::kOffV;
+    BwdBars* bars = reinterpret_cast<BwdBars*>(smem + L::kOffBars);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const BwdSeq sq = bwd_seq(p);
@@ -395,17 +519,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     const KvRange kr_ = kv_block_range(imin, imax, sq.Lq, sq.Lk, 128, p.causal, p.wl, p.wr);
     const int lo = kr_.lo, hi = kr_.hi;
 
+    // Rows of Q and dO past the packed tokens are never written by TMA: clear them once so
+    // that their S, dP and dS rows are zero.
+    for (int u = threadIdx.x; u < 2 * C::kTile / 16; u += blockDim.x)
+        st_shared_v4(smem_u32(sQ) + u * 16, 0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
     if (threadIdx.x == 0) {
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars->kv_full[s], 1);
-            mbar_init(&bars->kv_empty[s], 1);
-        }
-        mbar_init(&bars->q_full[0], 1);
-        mbar_init(&bars->s_full, 1);
-        mbar_init(&bars->p_full, 8);
-        mbar_init(&bars->mm_done, 1);
-        mbar_init(&bars->drain, 1);
-        bars->abort_flag = 0;
+        init_bars(bars);
         mbar_fence_init();
     }
     if (warp == 9) tmem_alloc(&bars->tmem_base, 512);
@@ -414,131 +534,160 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     const Watchdog wd{&bars->abort_flag, p.status};
-    // TMEM: S / dS [0, 128), dP [128, 256), dQ [256, 256 + D)
     constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
 
     if (warp == 8) {
+        regs_decrease<80>();
         if (lane == 0 && hi > lo) {
-            const uint32_t box = 64u * p.g * p.tpt * 2u * C::kHalves;
-            mbar_arrive_expect_tx(&bars->q_full[0], 2 * box);
+            const uint32_t box = 128u * p.g * p.tpt * C::kHalves;  // bytes of one operand
+            mbar_arrive_expect_tx(&bars->fixed_full, 2 * box);
 #pragma unroll
             for (int h = 0; h < C::kHalves; ++h) {
-                tma_load_3d(sQ + h * C::kAtomBytes, &p.tm_q, &bars->q_full[0], h * 64,
-                            sq.kvh * p.g, sq.q0 + imin);
-                tma_load_3d(sDO + h * C::kAtomBytes, &p.tm_do, &bars->q_full[0], h * 64,
+                tma_load_3d(sQ + h * C::kAtom, &p.tm_q, &bars->fixed_full, h * 64, sq.kvh * p.g,
+                            sq.q0 + imin);
+                tma_load_3d(sDO + h * C::kAtom, &p.tm_do, &bars->fixed_full, h * 64,
                             sq.kvh * p.g, sq.q0 + imin);
             }
-            uint32_t n = 0;
+            int n = 0;
             for (int j = lo; j < hi; ++j, ++n) {
-                const int s = n & 1;
-                if (n >= 2 && !wd.wait(&bars->kv_empty[s], ((n >> 1) - 1) & 1)) break;
-                mbar_arrive_expect_tx(&bars->kv_full[s], 2 * C::kTile);
+                const int st = n & 1;
+                if (n >= 2 && !wd.wait(&bars->in_empty[st], ((n >> 1) - 1) & 1)) break;
+                mbar_arrive_expect_tx(&bars->in_full[st], 2 * C::kTile);
 #pragma unroll
                 for (int h = 0; h < C::kHalves; ++h) {
-                    tma_load_3d(sK + s * C::kTile + h * C::kAtomBytes, &p.tm_k, &bars->kv_full[s],
+                    tma_load_3d(sK + st * C::kTile + h * C::kAtom, &p.tm_k, &bars->in_full[st],
                                 h * 64, sq.kvh, sq.k0 + j * 128);
-                    tma_load_3d(sV + s * C::kTile + h * C::kAtomBytes, &p.tm_v, &bars->kv_full[s],
+                    tma_load_3d(sV + st * C::kTile + h * C::kAtom, &p.tm_v, &bars->in_full[st],
                                 h * 64, sq.kvh, sq.k0 + j * 128);
                 }
             }
-            bwd_drain(&bars->q_full[0], 0);
-            for (uint32_t s = 0; s < 2 && s < n; ++s)
-                bwd_drain(&bars->kv_full[s], ((n - 1 - s) >> 1) & 1);
+            bwd_drain(&bars->fixed_full, 0);
+            for (int m = n > 2 ? n - 2 : 0; m < n; ++m) bwd_drain(&bars->in_full[m & 1], (m >> 1) & 1);
         }
     } else if (warp == 9) {
+        regs_decrease<80>();
         if (lane == 0) {
             constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
             constexpr uint32_t kIdG = idesc_bf16_f32(128, D, false, true);
             const uint64_t dq_ = sdesc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t ddo = sdesc_sw128(smem_u32(sDO), 16, 1024);
-            uint32_t n = 0;
-            if (hi > lo && wd.wait(&bars->q_full[0], 0)) {
-                for (int j = lo; j < hi; ++j, ++n) {
-                    const int s = n & 1;
-                    if (!wd.wait(&bars->kv_full[s], (n >> 1) & 1)) break;
-                    // S and dP overwrite dS of the previous block, which dQ read
-                    if (n > 0 && !wd.wait(&bars->mm_done, (n - 1) & 1)) break;
-                    tc_fence_after();
-                    const uint32_t k_base = smem_u32(sK + s * C::kTile);
-                    const uint64_t dk_ = sdesc_sw128(k_base, 16, 1024);
-                    const uint64_t dv_ = sdesc_sw128(smem_u32(sV + s * C::kTile), 16, 1024);
+            const uint64_t dds = sdesc_sw128(smem_u32(smem + L::kOffDS), 16, 1024);
+            // dQ += dS(m) K(m) (K in stage st): K-steps of 16 keys
+            auto grads = [&](int m, int st) {
+                if (!wd.wait(&bars->p_full[0], m & 1)) return false;
+                tc_fence_after();
+                const uint32_t k_base = smem_u32(sK + st * C::kTile);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t off = (((kk >> 2) * C::kAtomBytes + (kk & 3) * 32) >> 4);
-                        umma_ss(tmem + kColS, dq_ + off, dk_ + off, kIdS, kk > 0);
-                        umma_ss(tmem + kColDP, ddo + off, dv_ + off, kIdS, kk > 0);
-                    }
-                    umma_commit(&bars->s_full);
-                    if (!wd.wait(&bars->p_full, n & 1)) break;
-                    tc_fence_after();
+                for (int kk = 0; kk < 8; ++kk)
+                    umma_ss(tmem + kColDQ, dds + (((kk >> 2) * C::kAtom + (kk & 3) * 32) >> 4),
+                            sdesc_sw128(k_base + kk * 2048, C::kAtom, 1024), kIdG,
+                            (m > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&bars->p_empty);
+                umma_commit(&bars->in_empty[st]);
+                return true;
+            };
+            int n = 0, prev_st = 0;
+            bool ok = hi > lo && wd.wait(&bars->fixed_full, 0);
+            for (int j = lo; ok && j < hi; ++j) {
+                const int st = n & 1;
+                ok = wd.wait(&bars->in_full[st], (n >> 1) & 1);
+                // S(n), dP(n) over those of block n - 1, which are in registers
+                if (ok && n >= 1) ok = wd.wait(&bars->s_free, (n - 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t dk_ = sdesc_sw128(smem_u32(sK + st * C::kTile), 16, 1024);
+                const uint64_t dv_ = sdesc_sw128(smem_u32(sV + st * C::kTile), 16, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < 128 / 16; ++kk)
-                        umma_ts(tmem + kColDQ, tmem + kColS + kk * 8,
-                                sdesc_sw128(k_base + kk * 2048, C::kAtomBytes, 1024), kIdG,
-                                (n > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(&bars->mm_done);
-                    umma_commit(&bars->kv_empty[s]);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = (((kk >> 2) * C::kAtom + (kk & 3) * 32) >> 4);
+                    umma_ss(tmem + kColS, dq_ + off, dk_ + off, kIdS, kk > 0);
+                    umma_ss(tmem + kColDP, ddo + off, dv_ + off, kIdS, kk > 0);
                 }
+                umma_commit(&bars->s_full);
+                if (n >= 1 && !grads(n - 1, prev_st)) {
+                    ok = false;
+                    break;
+                }
+                prev_st = st;
+                ++n;
             }
+            if (ok && n >= 1) grads(n - 1, prev_st);
+            umma_commit(&bars->mm_done);
             umma_commit(&bars->drain);
             bwd_drain(&bars->drain, 0);
         }
-    } else if (warp < 8) {
+    } else if (warp >= 10) {
+        regs_decrease<80>();
+    } else {
+        regs_increase<208>();
         const int quarter = warp & 3, ch = warp >> 2;
         const int r = 32 * quarter + lane;  // packed row of the tile
         const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
-        if (threadIdx.x < 128) fill_rows(p, sq, i, true, info[0], threadIdx.x);
-        named_bar_sync(1, 256);
-        const float nl = info[0].nl[r], dd = info[0].dd[r];
-        const int kmin = info[0].kmin[r], kmax = info[0].kmax[r];
-        const bool row_valid = nl != -INFINITY;
-        bool ok = true;  // as in the dK/dV kernel: the named barrier is passed on every block
-        uint32_t n = 0;
+        const int tok = imin + r / p.g;
+        const bool in_tile = r < p.g * p.tpt && tok < sq.Lq;
+        float nl = -INFINITY, dd = 0.f;
+        int kmin = 1, kmax = 0;
+        if (in_tile) {
+            const size_t at = static_cast<size_t>(sq.kvh * p.g + r % p.g) * p.total_q + sq.q0 + tok;
+            const float l = p.lse[at];
+            if (l != -INFINITY) nl = -l * kLog2e;
+            dd = p.dsum[at];
+            row_key_interval(tok, sq.Lq, sq.Lk, p.causal, p.wl, p.wr, kmin, kmax);
+        }
+        const uint64_t scale2 = f2_make(p.scale_log2, p.scale_log2);
+        const uint64_t nl2 = f2_make(nl, nl), ndd2 = f2_make(-dd, -dd);
+        // This thread's row of the dS slot: keys 64 ch .. 64 ch + 63 are the 128-byte row r of
+        // atom ch, 16-byte chunk c at chunk c ^ (r % 8) (128-byte swizzle).
+        const uint32_t row_ds = smem_u32(smem + L::kOffDS) + ch * C::kAtom + r * 128;
+        bool ok = true;
+        int n = 0;
         for (int j = lo; j < hi; ++j, ++n) {
-            ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->s_full, n & 1));
-            tc_fence_after();
             const bool masked = kv_block_masked(j, imin, imax, sq.Lq, sq.Lk, 128, p.causal, p.wl,
                                                 p.wr);
-            uint32_t pd[32];
-#pragma unroll
-            for (int c2 = 0; c2 < 2 && ok; ++c2) {
-                const int col0 = 64 * ch + 32 * c2;
-                uint32_t sv[32], dv[32];
-                tmem_ld32(tmem + lane_off + kColS + col0, sv);
-                tmem_ld32(tmem + lane_off + kColDP + col0, dv);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float de[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int key = j * 128 + col0 + e + u;
-                        float x = fmaf(__uint_as_float(sv[e + u]), p.scale_log2, nl);
-                        if (masked && (key < kmin || key > kmax)) x = -INFINITY;
-                        const float pe = ex2_approx(x);
-                        de[u] = row_valid ? pe * (__uint_as_float(dv[e + u]) - dd) : 0.f;
-                    }
-                    pd[16 * c2 + e / 2] = pack_bf16x2(de[0], de[1]);
-                }
-            }
-            named_bar_sync(2, 256);
+            ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->s_full, n & 1));
+            tc_fence_after();
+            uint32_t sv[64], dv[64];
             if (ok) {
-                tmem_st32(tmem + lane_off + kColS + 32 * ch, pd);
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->p_full);
+                tmem_ld32(tmem + lane_off + kColS + 64 * ch, *reinterpret_cast<uint32_t(*)[32]>(sv));
+                tmem_ld32(tmem + lane_off + kColS + 64 * ch + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+                tmem_ld32(tmem + lane_off + kColDP + 64 * ch, *reinterpret_cast<uint32_t(*)[32]>(dv));
+                tmem_ld32(tmem + lane_off + kColDP + 64 * ch + 32, *reinterpret_cast<uint32_t(*)[32]>(dv + 32));
+                tmem_wait_ld();
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->s_free);
+            uint32_t pd[32];
+            const int key0 = j * 128 + 64 * ch;
+#pragma unroll
+            for (int e = 0; e < 64; e += 2) {
+                const bool m0 = masked && (key0 + e < kmin || key0 + e > kmax);
+                const bool m1 = masked && (key0 + e + 1 < kmin || key0 + e + 1 > kmax);
+                uint32_t pk;
+                p_ds_pair(sv[e], sv[e + 1], dv[e], dv[e + 1], scale2, nl2, ndd2, m0, m1, pk,
+                          pd[e / 2]);
+                (void)pk;
+            }
+            // the slot is free once dQ of block n - 1 has read it
+            if (n >= 1) ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->p_empty, (n - 1) & 1));
+            if (ok) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(row_ds + static_cast<uint32_t>((c ^ (r & 7)) * 16), pd[4 * c],
+                                 pd[4 * c + 1], pd[4 * c + 2], pd[4 * c + 3]);
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->p_full[0]);
         }
         // Epilogue: scale * dQ rows of this tile, bf16.
         if (n > 0) {
-            ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->mm_done, (n - 1) & 1));
+            ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->mm_done, 0));
             tc_fence_after();
         }
-        const int tok = imin + r / p.g;
-        const bool valid = ok && r < p.g * p.tpt && tok < sq.Lq;
-        __nv_bfloat16* dst = p.dq + (static_cast<size_t>(sq.q0 + tok) * p.Hq + sq.kvh * p.g + r % p.g) * D +
-                             (D / 2) * ch;
+        const bool valid = ok && in_tile;
+        __nv_bfloat16* dst =
+            p.dq + (static_cast<size_t>(sq.q0 + tok) * p.Hq + sq.kvh * p.g + r % p.g) * D + (D / 2) * ch;
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
             uint32_t o[32];
@@ -549,16 +698,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
 #pragma unroll
                 for (int e = 0; e < 32; ++e) o[e] = 0u;
             }
-            if (valid) {
-                uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
-#pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    d4[v] = make_uint4(
-                        pack_bf16x2(__uint_as_float(o[8 * v + 0]) * p.scale, __uint_as_float(o[8 * v + 1]) * p.scale),
-                        pack_bf16x2(__uint_as_float(o[8 * v + 2]) * p.scale, __uint_as_float(o[8 * v + 3]) * p.scale),
-                        pack_bf16x2(__uint_as_float(o[8 * v + 4]) * p.scale, __uint_as_float(o[8 * v + 5]) * p.scale),
-                        pack_bf16x2(__uint_as_float(o[8 * v + 6]) * p.scale, __uint_as_float(o[8 * v + 7]) * p.scale));
-            }
+            if (valid) store_row32(dst + 32 * c, o, p.scale);
         }
     }
     __syncwarp();
@@ -568,11 +708,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
-}
-
-template <int D>
-constexpr int bwd_smem() {
-    return 6 * BwdCfg<D>::kTile + 2 * static_cast<int>(sizeof(RowInfo)) + 256 + 1024;
 }
 
 }  // namespace
@@ -587,17 +722,17 @@ cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t stream) {
     const dim3 grid_kv((p.max_seqlen_k + 127) / 128, p.batch * p.Hkv);
     const dim3 grid_q((p.max_seqlen_q + p.tpt - 1) / p.tpt, p.batch * p.Hkv);
     if (p.d == 128) {
-        constexpr int sm = bwd_smem<128>();
-        cudaFuncSetAttribute(bwd_dkdv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-        cudaFuncSetAttribute(bwd_dq_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-        if (grid_kv.x > 0) bwd_dkdv_kernel<128><<<grid_kv, kBwdThreads, sm, stream>>>(p);
-        if (grid_q.x > 0) bwd_dq_kernel<128><<<grid_q, kBwdThreads, sm, stream>>>(p);
+        constexpr int a = DkdvSmem<128>::kBytes, b = DqSmem<128>::kBytes;
+        cudaFuncSetAttribute(bwd_dkdv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, a);
+        cudaFuncSetAttribute(bwd_dq_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, b);
+        if (grid_kv.x > 0) bwd_dkdv_kernel<128><<<grid_kv, kBwdThreads, a, stream>>>(p);
+        if (grid_q.x > 0) bwd_dq_kernel<128><<<grid_q, kBwdThreads, b, stream>>>(p);
     } else {
-        constexpr int sm = bwd_smem<64>();
-        cudaFuncSetAttribute(bwd_dkdv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-        cudaFuncSetAttribute(bwd_dq_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-        if (grid_kv.x > 0) bwd_dkdv_kernel<64><<<grid_kv, kBwdThreads, sm, stream>>>(p);
-        if (grid_q.x > 0) bwd_dq_kernel<64><<<grid_q, kBwdThreads, sm, stream>>>(p);
+        constexpr int a = DkdvSmem<64>::kBytes, b = DqSmem<64>::kBytes;
+        cudaFuncSetAttribute(bwd_dkdv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, a);
+        cudaFuncSetAttribute(bwd_dq_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, b);
+        if (grid_kv.x > 0) bwd_dkdv_kernel<64><<<grid_kv, kBwdThreads, a, stream>>>(p);
+        if (grid_q.x > 0) bwd_dq_kernel<64><<<grid_q, kBwdThreads, b, stream>>>(p);
     }
     return cudaGetLastError();
 }
