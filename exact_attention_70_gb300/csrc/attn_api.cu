@@ -466,15 +466,6 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
         encode_3d(&bp.tm_k, k, head_dim, nheads_kv, total_k > 0 ? total_k : 1, 1, 128) != ATTN_OK ||
         encode_3d(&bp.tm_v, v, head_dim, nheads_kv, total_k > 0 ? total_k : 1, 1, 128) != ATTN_OK)
         return ATTN_ERR_CUDA;
-    const int hb = g < 64 ? g : 64, tpt64 = g <= 64 ? 64 / g : 1;
-    if (encode_3d(&bp.tm_q64, q, head_dim, nheads_q, total_q > 0 ? total_q : 1, hb, tpt64) != ATTN_OK ||
-        encode_3d(&bp.tm_do64, dout, head_dim, nheads_q, total_q > 0 ? total_q : 1, hb, tpt64) != ATTN_OK ||
-        encode_3d(&bp.tm_k64, k, head_dim, nheads_kv, total_k > 0 ? total_k : 1, 1, 64) != ATTN_OK ||
-        encode_3d(&bp.tm_v64, v, head_dim, nheads_kv, total_k > 0 ? total_k : 1, 1, 64) != ATTN_OK)
-        return ATTN_ERR_CUDA;
-    bp.hb = hb;
-    bp.tpt64 = tpt64;
-    bp.sub = (g + 63) / 64;
     bp.o = static_cast<const __nv_bfloat16*>(out);
     bp.dout = static_cast<const __nv_bfloat16*>(dout);
     bp.lse = lse;

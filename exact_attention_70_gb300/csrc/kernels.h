@@ -95,14 +95,10 @@ int fwd_smem_bytes(int head_dim);
 // ---- backward ------------------------------------------------------------------------------
 
 struct BwdParams {
-    CUtensorMap tm_q;     // 3-D over q    [total_q, Hq, d], box {64, g, tpt}: 128-row Q tile
-    CUtensorMap tm_do;    // 3-D over dout [total_q, Hq, d], box {64, g, tpt}
-    CUtensorMap tm_k;     // 3-D over k    [total_k, Hkv, d], box {64, 1, 128}
+    CUtensorMap tm_q;   // 3-D over q    [total_q, Hq, d], box {64, g, tpt}
+    CUtensorMap tm_do;  // 3-D over dout [total_q, Hq, d], box {64, g, tpt}
+    CUtensorMap tm_k;   // 3-D over k    [total_k, Hkv, d], box {64, 1, 128}
     CUtensorMap tm_v;
-    CUtensorMap tm_q64;   // box {64, hb, tpt64}: 64-row Q sub-tile of the dK/dV kernel
-    CUtensorMap tm_do64;
-    CUtensorMap tm_k64;   // box {64, 1, 64}: 64-key block of the dQ kernel
-    CUtensorMap tm_v64;
     const __nv_bfloat16* o;     // [total_q, Hq, d]
     const __nv_bfloat16* dout;
     const float* lse;           // [Hq, total_q]
@@ -114,9 +110,6 @@ struct BwdParams {
     const int* cu_k;
     unsigned* status;
     int batch, Hq, Hkv, g, tpt, total_q, total_k, d, max_seqlen_q, max_seqlen_k;
-    // 64-row sub-tiles: hb = min(g, 64) heads by tpt64 tokens, and sub = ceil(g / 64) of them
-    // per token group (row r: token r / hb, head 64 * s + r % hb of sub-tile s)
-    int hb, tpt64, sub;
     int causal, wl, wr;
     float scale, scale_log2;
 };
