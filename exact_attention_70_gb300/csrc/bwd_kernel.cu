@@ -16,8 +16,8 @@
 //   Every MMA is 128 x 128 (x D) so the tensor pipe runs at its full rate.  The elementwise
 //   warps (0-7, two per TMEM lane quarter) pull S and dP of a block into registers first, which
 //   frees the TMEM region for the next block's MMA while they work; the gradient operand goes
-//   back as bf16 over dP^T in TMEM (dK/dV kernel) or to a 128-byte-swizzled shared-memory slot
-//   (dQ kernel).  Warp 9 issues the MMAs, warp 8 streams operands by TMA, and in the dK/dV
+//   back to TMEM as packed bf16 (over dP^T in the dK/dV kernel, into two spare slots in the dQ
+//   kernel) for MMAs that take their A operand from TMEM.  Warp 9 issues the MMAs, warp 8 streams operands by TMA, and in the dK/dV
 //   kernel warps 10-11 stage the query rows' L, D and key intervals a tile ahead.
 #include <cuda_bf16.h>
 
@@ -34,6 +34,7 @@ namespace {
 constexpr float kLog2e = 1.44269504088896341f;
 constexpr int kBwdThreads = 384;
 constexpr int kStages = 2;  // streamed operand ring (and row information ring)
+constexpr int kKStages = 3; // K ring of the dQ kernel
 
 template <int D>
 struct BwdCfg {
@@ -44,10 +45,11 @@ struct BwdCfg {
 
 struct BwdBars {
     uint64_t fixed_full;                               // loaded once (dK/dV: K, V; dQ: Q, dO)
-    uint64_t in_full[kStages], in_empty[kStages];      // streamed operands
+    uint64_t in_full[kKStages], in_empty[kKStages];    // streamed operands (dQ: K)
+    uint64_t v_full[kStages], v_empty[kStages];        // dQ: V
     uint64_t info_full[kStages], info_empty[kStages];  // row information (dK/dV)
     uint64_t s_full, s_free;                           // S / dP in TMEM, loaded to registers
-    uint64_t p_full[2], p_empty;                       // P^T, dS^T (TMEM) or dS (shared)
+    uint64_t p_full[2], p_empty[2];                    // P^T, dS^T or dS in TMEM
     uint64_t g_done, mm_done, drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -55,9 +57,13 @@ struct BwdBars {
 
 __device__ void init_bars(BwdBars* b) {
     mbar_init(&b->fixed_full, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
         mbar_init(&b->in_full[s], 1);
         mbar_init(&b->in_empty[s], 1);
+    }
+    for (int s = 0; s < kStages; ++s) {
+        mbar_init(&b->v_full[s], 1);
+        mbar_init(&b->v_empty[s], 1);
         mbar_init(&b->info_full[s], 64);
         mbar_init(&b->info_empty[s], 8);
     }
@@ -65,7 +71,8 @@ __device__ void init_bars(BwdBars* b) {
     mbar_init(&b->s_free, 8);
     mbar_init(&b->p_full[0], 8);
     mbar_init(&b->p_full[1], 8);
-    mbar_init(&b->p_empty, 1);
+    mbar_init(&b->p_empty[0], 1);
+    mbar_init(&b->p_empty[1], 1);
     mbar_init(&b->g_done, 1);
     mbar_init(&b->mm_done, 1);
     mbar_init(&b->drain, 1);
@@ -113,6 +120,17 @@ __device__ __forceinline__ void p_ds_pair(uint32_t s0, uint32_t s1, uint32_t dp0
     f2_split(f2_mul(pv, f2_add(f2_make(__uint_as_float(dp0), __uint_as_float(dp1)), ndd2)), d0, d1);
     p_out = pack_bf16x2(p0, p1);
     ds_out = pack_bf16x2(d0, d1);
+}
+
+// dS = exp2(s * scale_log2 + nl) (dp - dd) for two unmasked elements, packed as bf16.
+__device__ __forceinline__ uint32_t ds_pair(uint32_t s0, uint32_t s1, uint32_t dp0, uint32_t dp1,
+                                            uint64_t scale2, uint64_t nl2, uint64_t ndd2) {
+    float x0, x1;
+    f2_split(f2_fma(f2_make(__uint_as_float(s0), __uint_as_float(s1)), scale2, nl2), x0, x1);
+    const uint64_t pv = f2_make(ex2_approx(x0), ex2_approx(x1));
+    float d0, d1;
+    f2_split(f2_mul(pv, f2_add(f2_make(__uint_as_float(dp0), __uint_as_float(dp1)), ndd2)), d0, d1);
+    return pack_bf16x2(d0, d1);
 }
 
 // The sequence of (b, kvh) a CTA serves, checked against the tensors.
@@ -380,6 +398,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             const int st = n & 1;
             const bool masked = kv_block_masked(j, i * p.tpt, tok_hi(i), sq.Lq, sq.Lk, 128,
                                                 p.causal, p.wl, p.wr);
+            // row information is staged a tile ahead: take it before S^T
+            ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->info_full[st], (n >> 1) & 1));
             ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->s_full, n & 1));
             tc_fence_after();
             uint32_t sv[64];
@@ -391,7 +411,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->s_free);
-            ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->info_full[st], (n >> 1) & 1));
             const uint32_t ib = smem_u32(&info[st]);
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) {
@@ -401,12 +420,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
                     tmem_ld32(tmem + lane_off + col, dv);
                     tmem_wait_ld();
                     const uint32_t ibc = ib + 4 * (64 * ch + 32 * c2);
+                    if (!masked) {
+#pragma unroll
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const uint4 nl4 = ld_shared_v4(ibc + offsetof(RowInfo, nl) + 16 * e4);
+                            const uint4 dd4 = ld_shared_v4(ibc + offsetof(RowInfo, dd) + 16 * e4);
+                            const int e = 32 * c2 + 4 * e4;
+                            const uint64_t nla = f2_make(__uint_as_float(nl4.x), __uint_as_float(nl4.y));
+                            const uint64_t nlb = f2_make(__uint_as_float(nl4.z), __uint_as_float(nl4.w));
+                            float xa0, xa1, xb0, xb1;
+                            f2_split(f2_fma(f2_make(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), scale2, nla), xa0, xa1);
+                            f2_split(f2_fma(f2_make(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])), scale2, nlb), xb0, xb1);
+                            const uint64_t pa = f2_make(ex2_approx(xa0), ex2_approx(xa1));
+                            const uint64_t pb = f2_make(ex2_approx(xb0), ex2_approx(xb1));
+                            const uint64_t ta = f2_add(f2_make(__uint_as_float(dv[4 * e4]), __uint_as_float(dv[4 * e4 + 1])),
+                                                       f2_make(__uint_as_float(dd4.x), __uint_as_float(dd4.y)));
+                            const uint64_t tb = f2_add(f2_make(__uint_as_float(dv[4 * e4 + 2]), __uint_as_float(dv[4 * e4 + 3])),
+                                                       f2_make(__uint_as_float(dd4.z), __uint_as_float(dd4.w)));
+                            float p0, p1, p2, p3, d0, d1, d2, d3;
+                            f2_split(pa, p0, p1);
+                            f2_split(pb, p2, p3);
+                            f2_split(f2_mul(pa, ta), d0, d1);
+                            f2_split(f2_mul(pb, tb), d2, d3);
+                            pp[2 * e4] = pack_bf16x2(p0, p1);
+                            pp[2 * e4 + 1] = pack_bf16x2(p2, p3);
+                            pd[2 * e4] = pack_bf16x2(d0, d1);
+                            pd[2 * e4 + 1] = pack_bf16x2(d2, d3);
+                        }
+                    } else {
 #pragma unroll
                     for (int e4 = 0; e4 < 8; ++e4) {
                         const uint4 nl4 = ld_shared_v4(ibc + offsetof(RowInfo, nl) + 16 * e4);
                         const uint4 dd4 = ld_shared_v4(ibc + offsetof(RowInfo, dd) + 16 * e4);
-                        bool m[4] = {false, false, false, false};
-                        if (masked) {
+                        bool m[4];
+                        {
                             const uint4 lo4 = ld_shared_v4(ibc + offsetof(RowInfo, kmin) + 16 * e4);
                             const uint4 hi4 = ld_shared_v4(ibc + offsetof(RowInfo, kmax) + 16 * e4);
                             m[0] = key < static_cast<int>(lo4.x) || key > static_cast<int>(hi4.x);
@@ -423,6 +470,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
                                   f2_make(__uint_as_float(nl4.z), __uint_as_float(nl4.w)),
                                   f2_make(__uint_as_float(dd4.z), __uint_as_float(dd4.w)), m[2],
                                   m[3], pp[2 * e4 + 1], pd[2 * e4 + 1]);
+                    }
                     }
                     tmem_st16(tmem + lane_off + col, pp);
                     tmem_st16(tmem + lane_off + col + 16, pd);
@@ -474,22 +522,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
 // ---- dQ: one CTA per Q tile ---------------------------------------------------------------
 //
 // The CTA walks the 128-key blocks its 128 packed query rows see.  TMEM: S at [0, 128), dP at
-// [128, 256), dQ at [256, 256 + D).  Block n:
+// [128, 256), dQ at [256, 256 + D), two slots of packed bf16 dS at [384, 448) and [448, 512).
+// Block n:
 //   warps 0-7:  load their 64 columns of S(n) and dP(n) to registers (both regions are free
-//               again), form dS = P (dP - D) and write it as bf16 to the shared-memory slot;
+//               again), form dS = P (dP - D) and write it packed to slot n % 2;
 //   MMA warp:   S(n+1) = Q K(n+1)^T and dP(n+1) = dO V(n+1)^T as soon as S(n), dP(n) are in
-//               registers, then dQ += dS(n) K(n) with both operands in shared memory;
-//   warp 8:     TMA of Q, dO (once) and of K, V blocks (two stages).
+//               registers, then dQ += dS(n) K(n) with dS from TMEM;
+//   warp 8:     TMA of Q, dO (once), of K blocks into a three-stage ring (a K block is read
+//               until its dQ step) and of V blocks into a two-stage ring (read by dP only).
 
 template <int D>
 struct DqSmem {
     using C = BwdCfg<D>;
     static constexpr int kOffQ = 0;
     static constexpr int kOffDO = C::kTile;
-    static constexpr int kOffK = 2 * C::kTile;                // kStages stages
-    static constexpr int kOffV = kOffK + kStages * C::kTile;   // kStages stages
-    static constexpr int kOffDS = kOffV + kStages * C::kTile;  // 128 rows x 128 keys bf16
-    static constexpr int kOffBars = kOffDS + 2 * C::kAtom;
+    static constexpr int kOffK = 2 * C::kTile;                // kKStages stages
+    static constexpr int kOffV = kOffK + kKStages * C::kTile;  // kStages stages
+    static constexpr int kOffBars = kOffV + kStages * C::kTile;
     static constexpr int kBytes = kOffBars + static_cast<int>(sizeof(BwdBars)) + 1024;
 };
 static_assert(DqSmem<128>::kBytes <= 227 * 1024, "dQ shared memory");
@@ -534,7 +583,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     const Watchdog wd{&bars->abort_flag, p.status};
-    constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+    constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 384;
 
     if (warp == 8) {
         regs_decrease<80>();
@@ -548,21 +597,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
                 tma_load_3d(sDO + h * C::kAtom, &p.tm_do, &bars->fixed_full, h * 64,
                             sq.kvh * p.g, sq.q0 + imin);
             }
-            int n = 0;
-            for (int j = lo; j < hi; ++j, ++n) {
-                const int st = n & 1;
-                if (n >= 2 && !wd.wait(&bars->in_empty[st], ((n >> 1) - 1) & 1)) break;
-                mbar_arrive_expect_tx(&bars->in_full[st], 2 * C::kTile);
+            int nk = 0, nv = 0;  // K, V blocks loaded
+            for (int j = lo; j < hi; ++j) {
+                const int sk = nk % kKStages, sv = nv & 1;
+                if (nk >= kKStages && !wd.wait(&bars->in_empty[sk], ((nk / kKStages) - 1) & 1)) break;
+                mbar_arrive_expect_tx(&bars->in_full[sk], C::kTile);
 #pragma unroll
-                for (int h = 0; h < C::kHalves; ++h) {
-                    tma_load_3d(sK + st * C::kTile + h * C::kAtom, &p.tm_k, &bars->in_full[st],
+                for (int h = 0; h < C::kHalves; ++h)
+                    tma_load_3d(sK + sk * C::kTile + h * C::kAtom, &p.tm_k, &bars->in_full[sk],
                                 h * 64, sq.kvh, sq.k0 + j * 128);
-                    tma_load_3d(sV + st * C::kTile + h * C::kAtom, &p.tm_v, &bars->in_full[st],
+                ++nk;
+                if (nv >= 2 && !wd.wait(&bars->v_empty[sv], ((nv >> 1) - 1) & 1)) break;
+                mbar_arrive_expect_tx(&bars->v_full[sv], C::kTile);
+#pragma unroll
+                for (int h = 0; h < C::kHalves; ++h)
+                    tma_load_3d(sV + sv * C::kTile + h * C::kAtom, &p.tm_v, &bars->v_full[sv],
                                 h * 64, sq.kvh, sq.k0 + j * 128);
-                }
+                ++nv;
             }
             bwd_drain(&bars->fixed_full, 0);
-            for (int m = n > 2 ? n - 2 : 0; m < n; ++m) bwd_drain(&bars->in_full[m & 1], (m >> 1) & 1);
+            for (int m = nk > kKStages ? nk - kKStages : 0; m < nk; ++m)
+                bwd_drain(&bars->in_full[m % kKStages], (m / kKStages) & 1);
+            for (int m = nv > 2 ? nv - 2 : 0; m < nv; ++m) bwd_drain(&bars->v_full[m & 1], (m >> 1) & 1);
         }
     } else if (warp == 9) {
         regs_decrease<80>();
@@ -571,32 +627,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
             constexpr uint32_t kIdG = idesc_bf16_f32(128, D, false, true);
             const uint64_t dq_ = sdesc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t ddo = sdesc_sw128(smem_u32(sDO), 16, 1024);
-            const uint64_t dds = sdesc_sw128(smem_u32(smem + L::kOffDS), 16, 1024);
-            // dQ += dS(m) K(m) (K in stage st): K-steps of 16 keys
-            auto grads = [&](int m, int st) {
-                if (!wd.wait(&bars->p_full[0], m & 1)) return false;
+            // dQ += dS(m) K(m) (K in stage sk), dS from TMEM slot m % 2: K-steps of 16 keys,
+            // keys 64 c .. 64 c + 63 packed at slot + 32 c
+            auto grads = [&](int m, int sk) {
+                if (!wd.wait(&bars->p_full[m & 1], (m >> 1) & 1)) return false;
                 tc_fence_after();
-                const uint32_t k_base = smem_u32(sK + st * C::kTile);
+                const uint32_t k_base = smem_u32(sK + sk * C::kTile);
+                const uint32_t slot = kColDS + 64 * (m & 1);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    umma_ss(tmem + kColDQ, dds + (((kk >> 2) * C::kAtom + (kk & 3) * 32) >> 4),
+                    umma_ts(tmem + kColDQ, tmem + slot + 32 * (kk >> 2) + 8 * (kk & 3),
                             sdesc_sw128(k_base + kk * 2048, C::kAtom, 1024), kIdG,
                             (m > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&bars->p_empty);
-                umma_commit(&bars->in_empty[st]);
+                umma_commit(&bars->p_empty[m & 1]);
+                umma_commit(&bars->in_empty[sk]);
                 return true;
             };
-            int n = 0, prev_st = 0;
+            int n = 0, prev_sk = 0;
             bool ok = hi > lo && wd.wait(&bars->fixed_full, 0);
             for (int j = lo; ok && j < hi; ++j) {
-                const int st = n & 1;
-                ok = wd.wait(&bars->in_full[st], (n >> 1) & 1);
+                const int sk = n % kKStages, sv = n & 1;
+                ok = wd.wait(&bars->in_full[sk], (n / kKStages) & 1) &&
+                     wd.wait(&bars->v_full[sv], (n >> 1) & 1);
                 // S(n), dP(n) over those of block n - 1, which are in registers
                 if (ok && n >= 1) ok = wd.wait(&bars->s_free, (n - 1) & 1);
                 if (!ok) break;
                 tc_fence_after();
-                const uint64_t dk_ = sdesc_sw128(smem_u32(sK + st * C::kTile), 16, 1024);
-                const uint64_t dv_ = sdesc_sw128(smem_u32(sV + st * C::kTile), 16, 1024);
+                const uint64_t dk_ = sdesc_sw128(smem_u32(sK + sk * C::kTile), 16, 1024);
+                const uint64_t dv_ = sdesc_sw128(smem_u32(sV + sv * C::kTile), 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (((kk >> 2) * C::kAtom + (kk & 3) * 32) >> 4);
@@ -604,14 +662,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
                     umma_ss(tmem + kColDP, ddo + off, dv_ + off, kIdS, kk > 0);
                 }
                 umma_commit(&bars->s_full);
-                if (n >= 1 && !grads(n - 1, prev_st)) {
+                umma_commit(&bars->v_empty[sv]);
+                if (n >= 1 && !grads(n - 1, prev_sk)) {
                     ok = false;
                     break;
                 }
-                prev_st = st;
+                prev_sk = sk;
                 ++n;
             }
-            if (ok && n >= 1) grads(n - 1, prev_st);
+            if (ok && n >= 1) grads(n - 1, prev_sk);
             umma_commit(&bars->mm_done);
             umma_commit(&bars->drain);
             bwd_drain(&bars->drain, 0);
@@ -636,9 +695,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         }
         const uint64_t scale2 = f2_make(p.scale_log2, p.scale_log2);
         const uint64_t nl2 = f2_make(nl, nl), ndd2 = f2_make(-dd, -dd);
-        // This thread's row of the dS slot: keys 64 ch .. 64 ch + 63 are the 128-byte row r of
-        // atom ch, 16-byte chunk c at chunk c ^ (r % 8) (128-byte swizzle).
-        const uint32_t row_ds = smem_u32(smem + L::kOffDS) + ch * C::kAtom + r * 128;
         bool ok = true;
         int n = 0;
         for (int j = lo; j < hi; ++j, ++n) {
@@ -658,27 +714,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->s_free);
             uint32_t pd[32];
-            const int key0 = j * 128 + 64 * ch;
+            if (!masked) {
 #pragma unroll
-            for (int e = 0; e < 64; e += 2) {
-                const bool m0 = masked && (key0 + e < kmin || key0 + e > kmax);
-                const bool m1 = masked && (key0 + e + 1 < kmin || key0 + e + 1 > kmax);
-                uint32_t pk;
-                p_ds_pair(sv[e], sv[e + 1], dv[e], dv[e + 1], scale2, nl2, ndd2, m0, m1, pk,
-                          pd[e / 2]);
-                (void)pk;
+                for (int e = 0; e < 64; e += 2)
+                    pd[e / 2] = ds_pair(sv[e], sv[e + 1], dv[e], dv[e + 1], scale2, nl2, ndd2);
+            } else {
+                const int k0 = j * 128 + 64 * ch;
+#pragma unroll
+                for (int e = 0; e < 64; e += 2) {
+                    uint32_t pk;
+                    p_ds_pair(sv[e], sv[e + 1], dv[e], dv[e + 1], scale2, nl2, ndd2,
+                              k0 + e < kmin || k0 + e > kmax, k0 + e + 1 < kmin || k0 + e + 1 > kmax,
+                              pk, pd[e / 2]);
+                    (void)pk;
+                }
             }
-            // the slot is free once dQ of block n - 1 has read it
-            if (n >= 1) ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->p_empty, (n - 1) & 1));
+            // slot n % 2 is free once dQ of block n - 2 has read it
+            if (n >= 2)
+                ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->p_empty[n & 1], ((n - 2) >> 1) & 1));
             if (ok) {
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    st_shared_v4(row_ds + static_cast<uint32_t>((c ^ (r & 7)) * 16), pd[4 * c],
-                                 pd[4 * c + 1], pd[4 * c + 2], pd[4 * c + 3]);
-                fence_proxy_async_smem();
+                tmem_st32(tmem + lane_off + kColDS + 64 * (n & 1) + 32 * ch, pd);
+                tmem_wait_st();
             }
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->p_full[0]);
+            if (lane == 0) mbar_arrive(&bars->p_full[n & 1]);
         }
         // Epilogue: scale * dQ rows of this tile, bf16.
         if (n > 0) {
