@@ -14,11 +14,13 @@
 //     128-row Q tiles (tokens x query heads, packed as in the forward pass) that see it;
 //   * bwd_dq_kernel: one CTA per 128-row Q tile, walking the 128-key blocks it sees.
 //   Every MMA is 128 x 128 (x D) so the tensor pipe runs at its full rate.  The elementwise
-//   warps (0-7, two per TMEM lane quarter) pull S and dP of a block into registers first, which
-//   frees the TMEM region for the next block's MMA while they work; the gradient operand goes
-//   back to TMEM as packed bf16 (over dP^T in the dK/dV kernel, into two spare slots in the dQ
-//   kernel) for MMAs that take their A operand from TMEM.  Warp 9 issues the MMAs, warp 8 streams operands by TMA, and in the dK/dV
-//   kernel warps 10-11 stage the query rows' L, D and key intervals a tile ahead.
+//   warps (0-7, two per TMEM lane quarter) pull S and dP of a block into registers, which
+//   frees that TMEM for the next MMA while they work; the gradient operand goes back to TMEM
+//   as packed bf16 (over S^T and dP^T in the dK/dV kernel, into two spare slots in the dQ
+//   kernel) for MMAs that take their A operand from TMEM.  Two warps issue MMAs, one per
+//   stream (9: S and dP; 11: the gradients), so neither stream waits behind the other; warp 8
+//   streams operands by TMA, and in the dK/dV kernel warp 10 stages the query rows' L, D and
+//   key intervals a tile ahead.
 #include <cuda_bf16.h>
 
 #include <cstddef>
@@ -48,9 +50,11 @@ struct BwdBars {
     uint64_t in_full[kKStages], in_empty[kKStages];    // streamed operands (dQ: K)
     uint64_t v_full[kStages], v_empty[kStages];        // dQ: V
     uint64_t info_full[kStages], info_empty[kStages];  // row information (dK/dV)
-    uint64_t s_full, s_free;                           // S / dP in TMEM, loaded to registers
-    uint64_t p_full[2], p_empty[2];                    // P^T, dS^T or dS in TMEM
-    uint64_t g_done, mm_done, drain;
+    uint64_t s_full, s_free;                           // dQ: S / dP in TMEM, loaded to registers
+    uint64_t p_full[2], p_empty[2];                    // dQ: dS slots in TMEM
+    uint64_t sa_full, sb_full, pa_full, pb_full;       // dK/dV: S^T, dP^T in; P^T, dS^T out
+    uint64_t dv_done, dk_done;                         // dK/dV: gradient MMAs have read P^T / dS^T
+    uint64_t mm_done, drain[2];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -64,7 +68,7 @@ __device__ void init_bars(BwdBars* b) {
     for (int s = 0; s < kStages; ++s) {
         mbar_init(&b->v_full[s], 1);
         mbar_init(&b->v_empty[s], 1);
-        mbar_init(&b->info_full[s], 64);
+        mbar_init(&b->info_full[s], 32);
         mbar_init(&b->info_empty[s], 8);
     }
     mbar_init(&b->s_full, 1);
@@ -73,9 +77,15 @@ __device__ void init_bars(BwdBars* b) {
     mbar_init(&b->p_full[1], 8);
     mbar_init(&b->p_empty[0], 1);
     mbar_init(&b->p_empty[1], 1);
-    mbar_init(&b->g_done, 1);
+    mbar_init(&b->sa_full, 1);
+    mbar_init(&b->sb_full, 1);
+    mbar_init(&b->pa_full, 8);
+    mbar_init(&b->pb_full, 8);
+    mbar_init(&b->dv_done, 1);
+    mbar_init(&b->dk_done, 1);
     mbar_init(&b->mm_done, 1);
-    mbar_init(&b->drain, 1);
+    mbar_init(&b->drain[0], 1);
+    mbar_init(&b->drain[1], 1);
     b->abort_flag = 0;
 }
 
@@ -179,17 +189,21 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
 
 // ---- dK, dV: one CTA per key block --------------------------------------------------------
 //
-// The CTA walks the 128-row Q tiles that see key block j.  TMEM: S^T at [0, 128), dP^T at
-// [128, 256), dV at [256, 256 + D), dK at [256 + D, 256 + 2 D).  Tile n:
-//   warps 0-7:   load their 64 columns of S^T(n) to registers (the S^T region is free again),
-//                then per 32-column chunk load dP^T, form P^T = exp2(S^T scale log2(e) -
-//                L log2(e)) and dS^T = P^T (dP^T - D), and write both as packed bf16 over the
-//                chunk's own dP^T columns (P^T in the first 16, dS^T in the last 16);
-//   MMA warp:    S^T(n+1) = K Q(n+1)^T as soon as S^T(n) is in registers; dV += P^T dO and
-//                dK += dS^T Q (A from TMEM) in two halves as the chunks arrive; dP^T(n+1) =
-//                V dO(n+1)^T once those have read the dP^T region;
-//   warps 10-11: the rows' -L log2(e), D and key intervals, a tile ahead;
+// The CTA walks the 128-row Q tiles that see key block j.  TMEM: region F = [0, 128) holds
+// S^T and then packed P^T, region G = [128, 256) holds dP^T and then packed dS^T, dV is at
+// [256, 256 + D) and dK at [256 + D, 256 + 2 D).  Tile n:
+//   warps 0-7:   phase A: their 64 columns of S^T to registers, P^T = exp2(S^T scale log2(e) -
+//                L log2(e)) kept in fp32, packed bf16 P^T over their own S^T columns;
+//                phase B: per 32-column chunk of dP^T, dS^T = P^T (dP^T - D), packed bf16 over
+//                the chunk's own dP^T columns;
+//   warp 9:      S^T(n) = K Q(n)^T into F once dV(n-1) has read P^T(n-1), then dP^T(n) =
+//                V dO(n)^T into G once dK(n-1) has read dS^T(n-1);
+//   warp 11:     dV += P^T(n) dO(n) after phase A and dK += dS^T(n) Q(n) after phase B, with
+//                A from TMEM;
+//   warp 10:     the rows' -L log2(e), D and key intervals, a tile ahead;
 //   warp 8:      TMA of K, V (once) and of Q, dO tiles (two stages).
+// So the tensor pipe runs S^T, dP^T, dV, dK of one tile back to back while the elementwise
+// warps work phase by phase.
 
 template <int D>
 struct DkdvSmem {
@@ -250,7 +264,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     const Watchdog wd{&bars->abort_flag, p.status};
-    constexpr uint32_t kColS = 0, kColG = 128, kColDV = 256, kColDK = 256 + D;
+    constexpr uint32_t kColF = 0, kColG = 128, kColDV = 256, kColDK = 256 + D;
+    constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t kIdG = idesc_bf16_f32(128, D, false, true);
 
     // Registers: launched at 168 per thread; warps 8-11 drop to 80 and the elementwise warps
     // rise to 208: 128 * 80 + 256 * 208 = 63488 <= 384 * 168.  (Each role sets its own count.)
@@ -289,82 +305,88 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     } else if (warp == 9) {
         regs_decrease<80>();
         if (lane == 0) {
-            constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
-            constexpr uint32_t kIdG = idesc_bf16_f32(128, D, false, true);
-            const uint64_t dk_ = sdesc_sw128(smem_u32(sK), 16, 1024);
-            const uint64_t dv_ = sdesc_sw128(smem_u32(sV), 16, 1024);
             // X^T = A B^T over d into TMEM column col, B a Q / dO stage
-            auto s_mma = [&](uint32_t col, uint64_t a, const uint8_t* b) {
+            auto s_mma = [&](uint32_t col, const uint8_t* a, const uint8_t* b) {
+                const uint64_t ad = sdesc_sw128(smem_u32(a), 16, 1024);
                 const uint64_t bd = sdesc_sw128(smem_u32(b), 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (((kk >> 2) * C::kAtom + (kk & 3) * 32) >> 4);
-                    umma_ss(tmem + col, a + off, bd + off, kIdS, kk > 0);
+                    umma_ss(tmem + col, ad + off, bd + off, kIdS, kk > 0);
                 }
             };
-            // dV += P^T dO, dK += dS^T Q of tile m (stage st), K-steps of query rows 16 kk:
-            // half h holds the steps kk with (kk >> 1) & 1 == h, written by the chunk c2 == h
-            // of both column halves
-            auto grads = [&](int m, int st) {
-                const uint32_t q_base = smem_u32(sQ + st * C::kTile);
-                const uint32_t do_base = smem_u32(sDO + st * C::kTile);
-                for (int h = 0; h < 2; ++h) {
-                    if (!wd.wait(&bars->p_full[h], m & 1)) return false;
-                    tc_fence_after();
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int kk = 4 * (u >> 1) + 2 * h + (u & 1);
-                        const uint32_t a_col = kColG + 32 * (kk >> 1) + 8 * (kk & 1);
-                        const uint32_t acc = (m > 0 || u > 0 || h > 0) ? 1u : 0u;
-                        umma_ts(tmem + kColDV, tmem + a_col,
-                                sdesc_sw128(do_base + kk * 2048, C::kAtom, 1024), kIdG, acc);
-                        umma_ts(tmem + kColDK, tmem + a_col + 16,
-                                sdesc_sw128(q_base + kk * 2048, C::kAtom, 1024), kIdG, acc);
-                    }
-                }
-                umma_commit(&bars->g_done);
-                umma_commit(&bars->in_empty[st]);
-                return true;
-            };
-            int n = 0, prev_st = 0;
+            int n = 0;
             bool ok = wd.wait(&bars->fixed_full, 0);
             for (int i = 0; ok && i < n_qt; ++i) {
                 if (!sees(i)) continue;
                 const int st = n & 1;
-                ok = wd.wait(&bars->in_full[st], (n >> 1) & 1);
-                // S^T(n) over S^T(n-1), which the elementwise warps have in registers
-                if (ok && n >= 1) ok = wd.wait(&bars->s_free, (n - 1) & 1);
+                // S^T(n) into F once dV(n-1) has read P^T(n-1)
+                ok = wd.wait(&bars->in_full[st], (n >> 1) & 1) &&
+                     (n == 0 || wd.wait(&bars->dv_done, (n - 1) & 1));
                 if (!ok) break;
                 tc_fence_after();
-                s_mma(kColS, dk_, sQ + st * C::kTile);
-                // dP^T(n) over P^T, dS^T of tile n - 1 once dV, dK have read them
-                if (n >= 1) {
-                    ok = grads(n - 1, prev_st) && wd.wait(&bars->g_done, (n - 1) & 1);
-                    if (!ok) break;
-                    tc_fence_after();
-                }
-                s_mma(kColG, dv_, sDO + st * C::kTile);
-                umma_commit(&bars->s_full);
-                prev_st = st;
+                s_mma(kColF, sK, sQ + st * C::kTile);
+                umma_commit(&bars->sa_full);
+                // dP^T(n) into G once dK(n-1) has read dS^T(n-1)
+                ok = n == 0 || wd.wait(&bars->dk_done, (n - 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                s_mma(kColG, sV, sDO + st * C::kTile);
+                umma_commit(&bars->sb_full);
                 ++n;
             }
-            if (ok && n >= 1) grads(n - 1, prev_st);
-            umma_commit(&bars->mm_done);
-            umma_commit(&bars->drain);
-            bwd_drain(&bars->drain, 0);
+            umma_commit(&bars->drain[0]);
+            bwd_drain(&bars->drain[0], 0);
         }
-    } else if (warp >= 10) {
+    } else if (warp == 11) {
         regs_decrease<80>();
-        // Row information of each tile: thread r fills packed rows r and r + 64.
-        const int r0 = threadIdx.x - 320;
+        if (lane == 0) {
+            int n = 0;
+            bool ok = true;
+            for (int i = 0; ok && i < n_qt; ++i) {
+                if (!sees(i)) continue;
+                const int st = n & 1;
+                const uint32_t q_base = smem_u32(sQ + st * C::kTile);
+                const uint32_t do_base = smem_u32(sDO + st * C::kTile);
+                // dV += P^T dO: K-step kk (query rows 16 kk ..) packed at F + 64 (kk / 4) +
+                // 8 (kk % 4)
+                ok = wd.wait(&bars->pa_full, n & 1);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    umma_ts(tmem + kColDV, tmem + kColF + 64 * (kk >> 2) + 8 * (kk & 3),
+                            sdesc_sw128(do_base + kk * 2048, C::kAtom, 1024), kIdG,
+                            (n > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&bars->dv_done);
+                // dK += dS^T Q: K-step kk packed at G + 32 (kk / 2) + 8 (kk % 2)
+                ok = wd.wait(&bars->pb_full, n & 1);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    umma_ts(tmem + kColDK, tmem + kColG + 32 * (kk >> 1) + 8 * (kk & 1),
+                            sdesc_sw128(q_base + kk * 2048, C::kAtom, 1024), kIdG,
+                            (n > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&bars->dk_done);
+                umma_commit(&bars->in_empty[st]);
+                ++n;
+            }
+            umma_commit(&bars->mm_done);
+            umma_commit(&bars->drain[1]);
+            bwd_drain(&bars->drain[1], 0);
+        }
+    } else if (warp == 10) {
+        regs_decrease<80>();
+        // Row information of each tile: lane l fills packed rows l, l + 32, l + 64, l + 96.
         int n = 0;
         for (int i = 0; i < n_qt; ++i) {
             if (!sees(i)) continue;
             const int st = n & 1;
             if (n >= 2 && !wd.wait(&bars->info_empty[st], ((n >> 1) - 1) & 1)) break;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int r = r0 + 64 * h;
+            for (int h = 0; h < 4; ++h) {
+                const int r = lane + 32 * h;
                 const int tok = i * p.tpt + r / p.g;
                 float nl = -INFINITY, dd = 0.f;
                 int kmin = 1, kmax = 0;
@@ -398,90 +420,102 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             const int st = n & 1;
             const bool masked = kv_block_masked(j, i * p.tpt, tok_hi(i), sq.Lq, sq.Lk, 128,
                                                 p.causal, p.wl, p.wr);
-            // row information is staged a tile ahead: take it before S^T
+            // this warp's 64 query rows (columns) of the row information
+            const uint32_t ib = smem_u32(&info[st]) + 4 * 64 * ch;
             ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->info_full[st], (n >> 1) & 1));
-            ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->s_full, n & 1));
+            // phase A: P^T from S^T
+            ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->sa_full, n & 1));
             tc_fence_after();
-            uint32_t sv[64];
+            uint32_t pv[64];  // S^T, then P^T in fp32
             if (ok) {
-                tmem_ld32(tmem + lane_off + kColS + 64 * ch, *reinterpret_cast<uint32_t(*)[32]>(sv));
-                tmem_ld32(tmem + lane_off + kColS + 64 * ch + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+                tmem_ld32(tmem + lane_off + kColF + 64 * ch, *reinterpret_cast<uint32_t(*)[32]>(pv));
+                tmem_ld32(tmem + lane_off + kColF + 64 * ch + 32, *reinterpret_cast<uint32_t(*)[32]>(pv + 32));
                 tmem_wait_ld();
+                if (!masked) {
+#pragma unroll
+                    for (int e4 = 0; e4 < 16; ++e4) {
+                        const uint4 nl4 = ld_shared_v4(ib + offsetof(RowInfo, nl) + 16 * e4);
+                        const int e = 4 * e4;
+                        float x0, x1, x2, x3;
+                        f2_split(f2_fma(f2_make(__uint_as_float(pv[e]), __uint_as_float(pv[e + 1])), scale2,
+                                        f2_make(__uint_as_float(nl4.x), __uint_as_float(nl4.y))), x0, x1);
+                        f2_split(f2_fma(f2_make(__uint_as_float(pv[e + 2]), __uint_as_float(pv[e + 3])), scale2,
+                                        f2_make(__uint_as_float(nl4.z), __uint_as_float(nl4.w))), x2, x3);
+                        pv[e] = __float_as_uint(ex2_approx(x0));
+                        pv[e + 1] = __float_as_uint(ex2_approx(x1));
+                        pv[e + 2] = __float_as_uint(ex2_approx(x2));
+                        pv[e + 3] = __float_as_uint(ex2_approx(x3));
+                    }
+                } else {
+#pragma unroll
+                    for (int e4 = 0; e4 < 16; ++e4) {
+                        const uint4 nl4 = ld_shared_v4(ib + offsetof(RowInfo, nl) + 16 * e4);
+                        const uint4 lo4 = ld_shared_v4(ib + offsetof(RowInfo, kmin) + 16 * e4);
+                        const uint4 hi4 = ld_shared_v4(ib + offsetof(RowInfo, kmax) + 16 * e4);
+                        const uint32_t nlv[4] = {nl4.x, nl4.y, nl4.z, nl4.w};
+                        const uint32_t lov[4] = {lo4.x, lo4.y, lo4.z, lo4.w};
+                        const uint32_t hiv[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int e = 4 * e4 + u;
+                            const bool vis = key >= static_cast<int>(lov[u]) && key <= static_cast<int>(hiv[u]);
+                            const float x = fmaf(__uint_as_float(pv[e]), p.scale_log2, __uint_as_float(nlv[u]));
+                            pv[e] = __float_as_uint(ex2_approx(vis ? x : -INFINITY));
+                        }
+                    }
+                }
+                // packed query columns 64 ch + 2 c, 2 c + 1 at F + 64 ch + c: own columns
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pp[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        pp[c] = pack_bf16x2(__uint_as_float(pv[32 * h + 2 * c]),
+                                            __uint_as_float(pv[32 * h + 2 * c + 1]));
+                    tmem_st16(tmem + lane_off + kColF + 64 * ch + 16 * h, pp);
+                }
+                tmem_wait_st();
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->s_free);
-            const uint32_t ib = smem_u32(&info[st]);
+            if (lane == 0) mbar_arrive(&bars->pa_full);
+            // phase B: dS^T from dP^T
+            ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->sb_full, n & 1));
+            tc_fence_after();
+            if (ok) {
 #pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-                const uint32_t col = kColG + 64 * ch + 32 * c2;
-                if (ok) {
-                    uint32_t dv[32], pp[16], pd[16];
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    const uint32_t col = kColG + 64 * ch + 32 * c2;
+                    uint32_t dv[32], pd[16];
                     tmem_ld32(tmem + lane_off + col, dv);
                     tmem_wait_ld();
-                    const uint32_t ibc = ib + 4 * (64 * ch + 32 * c2);
-                    if (!masked) {
-#pragma unroll
-                        for (int e4 = 0; e4 < 8; ++e4) {
-                            const uint4 nl4 = ld_shared_v4(ibc + offsetof(RowInfo, nl) + 16 * e4);
-                            const uint4 dd4 = ld_shared_v4(ibc + offsetof(RowInfo, dd) + 16 * e4);
-                            const int e = 32 * c2 + 4 * e4;
-                            const uint64_t nla = f2_make(__uint_as_float(nl4.x), __uint_as_float(nl4.y));
-                            const uint64_t nlb = f2_make(__uint_as_float(nl4.z), __uint_as_float(nl4.w));
-                            float xa0, xa1, xb0, xb1;
-                            f2_split(f2_fma(f2_make(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), scale2, nla), xa0, xa1);
-                            f2_split(f2_fma(f2_make(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])), scale2, nlb), xb0, xb1);
-                            const uint64_t pa = f2_make(ex2_approx(xa0), ex2_approx(xa1));
-                            const uint64_t pb = f2_make(ex2_approx(xb0), ex2_approx(xb1));
-                            const uint64_t ta = f2_add(f2_make(__uint_as_float(dv[4 * e4]), __uint_as_float(dv[4 * e4 + 1])),
-                                                       f2_make(__uint_as_float(dd4.x), __uint_as_float(dd4.y)));
-                            const uint64_t tb = f2_add(f2_make(__uint_as_float(dv[4 * e4 + 2]), __uint_as_float(dv[4 * e4 + 3])),
-                                                       f2_make(__uint_as_float(dd4.z), __uint_as_float(dd4.w)));
-                            float p0, p1, p2, p3, d0, d1, d2, d3;
-                            f2_split(pa, p0, p1);
-                            f2_split(pb, p2, p3);
-                            f2_split(f2_mul(pa, ta), d0, d1);
-                            f2_split(f2_mul(pb, tb), d2, d3);
-                            pp[2 * e4] = pack_bf16x2(p0, p1);
-                            pp[2 * e4 + 1] = pack_bf16x2(p2, p3);
-                            pd[2 * e4] = pack_bf16x2(d0, d1);
-                            pd[2 * e4 + 1] = pack_bf16x2(d2, d3);
-                        }
-                    } else {
 #pragma unroll
                     for (int e4 = 0; e4 < 8; ++e4) {
-                        const uint4 nl4 = ld_shared_v4(ibc + offsetof(RowInfo, nl) + 16 * e4);
-                        const uint4 dd4 = ld_shared_v4(ibc + offsetof(RowInfo, dd) + 16 * e4);
-                        bool m[4];
-                        {
-                            const uint4 lo4 = ld_shared_v4(ibc + offsetof(RowInfo, kmin) + 16 * e4);
-                            const uint4 hi4 = ld_shared_v4(ibc + offsetof(RowInfo, kmax) + 16 * e4);
-                            m[0] = key < static_cast<int>(lo4.x) || key > static_cast<int>(hi4.x);
-                            m[1] = key < static_cast<int>(lo4.y) || key > static_cast<int>(hi4.y);
-                            m[2] = key < static_cast<int>(lo4.z) || key > static_cast<int>(hi4.z);
-                            m[3] = key < static_cast<int>(lo4.w) || key > static_cast<int>(hi4.w);
-                        }
+                        const uint4 dd4 = ld_shared_v4(ib + offsetof(RowInfo, dd) + 4 * 32 * c2 + 16 * e4);
                         const int e = 32 * c2 + 4 * e4;
-                        p_ds_pair(sv[e], sv[e + 1], dv[4 * e4], dv[4 * e4 + 1], scale2,
-                                  f2_make(__uint_as_float(nl4.x), __uint_as_float(nl4.y)),
-                                  f2_make(__uint_as_float(dd4.x), __uint_as_float(dd4.y)), m[0],
-                                  m[1], pp[2 * e4], pd[2 * e4]);
-                        p_ds_pair(sv[e + 2], sv[e + 3], dv[4 * e4 + 2], dv[4 * e4 + 3], scale2,
-                                  f2_make(__uint_as_float(nl4.z), __uint_as_float(nl4.w)),
-                                  f2_make(__uint_as_float(dd4.z), __uint_as_float(dd4.w)), m[2],
-                                  m[3], pp[2 * e4 + 1], pd[2 * e4 + 1]);
+                        float d[4];
+                        f2_split(f2_mul(f2_make(__uint_as_float(pv[e]), __uint_as_float(pv[e + 1])),
+                                        f2_add(f2_make(__uint_as_float(dv[4 * e4]), __uint_as_float(dv[4 * e4 + 1])),
+                                               f2_make(__uint_as_float(dd4.x), __uint_as_float(dd4.y)))),
+                                 d[0], d[1]);
+                        f2_split(f2_mul(f2_make(__uint_as_float(pv[e + 2]), __uint_as_float(pv[e + 3])),
+                                        f2_add(f2_make(__uint_as_float(dv[4 * e4 + 2]), __uint_as_float(dv[4 * e4 + 3])),
+                                               f2_make(__uint_as_float(dd4.z), __uint_as_float(dd4.w)))),
+                                 d[2], d[3]);
+                        pd[2 * e4] = pack_bf16x2(d[0], d[1]);
+                        pd[2 * e4 + 1] = pack_bf16x2(d[2], d[3]);
                     }
-                    }
-                    tmem_st16(tmem + lane_off + col, pp);
-                    tmem_st16(tmem + lane_off + col + 16, pd);
-                    tmem_wait_st();
+                    // packed into the first 16 of the chunk's own 32 dP^T columns
+                    tmem_st16(tmem + lane_off + col, pd);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->p_full[c2]);
+                tmem_wait_st();
             }
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->info_empty[st]);
+            if (lane == 0) {
+                mbar_arrive(&bars->pb_full);
+                mbar_arrive(&bars->info_empty[st]);
+            }
             ++n;
         }
         // Epilogue: dV and scale * dK rows of this key block, bf16.
@@ -526,8 +560,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
 // Block n:
 //   warps 0-7:  load their 64 columns of S(n) and dP(n) to registers (both regions are free
 //               again), form dS = P (dP - D) and write it packed to slot n % 2;
-//   MMA warp:   S(n+1) = Q K(n+1)^T and dP(n+1) = dO V(n+1)^T as soon as S(n), dP(n) are in
-//               registers, then dQ += dS(n) K(n) with dS from TMEM;
+//   warp 9:     S(n+1) = Q K(n+1)^T and dP(n+1) = dO V(n+1)^T as soon as S(n), dP(n) are in
+//               registers;
+//   warp 11:    dQ += dS(n) K(n) with dS from TMEM;
 //   warp 8:     TMA of Q, dO (once), of K blocks into a three-stage ring (a K block is read
 //               until its dQ step) and of V blocks into a two-stage ring (read by dP only).
 
@@ -623,34 +658,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     } else if (warp == 9) {
         regs_decrease<80>();
         if (lane == 0) {
+            // S(n) = Q K(n)^T, dP(n) = dO V(n)^T once S(n-1), dP(n-1) are in registers
             constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
-            constexpr uint32_t kIdG = idesc_bf16_f32(128, D, false, true);
             const uint64_t dq_ = sdesc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t ddo = sdesc_sw128(smem_u32(sDO), 16, 1024);
-            // dQ += dS(m) K(m) (K in stage sk), dS from TMEM slot m % 2: K-steps of 16 keys,
-            // keys 64 c .. 64 c + 63 packed at slot + 32 c
-            auto grads = [&](int m, int sk) {
-                if (!wd.wait(&bars->p_full[m & 1], (m >> 1) & 1)) return false;
-                tc_fence_after();
-                const uint32_t k_base = smem_u32(sK + sk * C::kTile);
-                const uint32_t slot = kColDS + 64 * (m & 1);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    umma_ts(tmem + kColDQ, tmem + slot + 32 * (kk >> 2) + 8 * (kk & 3),
-                            sdesc_sw128(k_base + kk * 2048, C::kAtom, 1024), kIdG,
-                            (m > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&bars->p_empty[m & 1]);
-                umma_commit(&bars->in_empty[sk]);
-                return true;
-            };
-            int n = 0, prev_sk = 0;
+            int n = 0;
             bool ok = hi > lo && wd.wait(&bars->fixed_full, 0);
-            for (int j = lo; ok && j < hi; ++j) {
+            for (int j = lo; ok && j < hi; ++j, ++n) {
                 const int sk = n % kKStages, sv = n & 1;
                 ok = wd.wait(&bars->in_full[sk], (n / kKStages) & 1) &&
-                     wd.wait(&bars->v_full[sv], (n >> 1) & 1);
-                // S(n), dP(n) over those of block n - 1, which are in registers
-                if (ok && n >= 1) ok = wd.wait(&bars->s_free, (n - 1) & 1);
+                     wd.wait(&bars->v_full[sv], (n >> 1) & 1) &&
+                     (n == 0 || wd.wait(&bars->s_free, (n - 1) & 1));
                 if (!ok) break;
                 tc_fence_after();
                 const uint64_t dk_ = sdesc_sw128(smem_u32(sK + sk * C::kTile), 16, 1024);
@@ -663,19 +681,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
                 }
                 umma_commit(&bars->s_full);
                 umma_commit(&bars->v_empty[sv]);
-                if (n >= 1 && !grads(n - 1, prev_sk)) {
-                    ok = false;
-                    break;
-                }
-                prev_sk = sk;
-                ++n;
             }
-            if (ok && n >= 1) grads(n - 1, prev_sk);
-            umma_commit(&bars->mm_done);
-            umma_commit(&bars->drain);
-            bwd_drain(&bars->drain, 0);
+            umma_commit(&bars->drain[0]);
+            bwd_drain(&bars->drain[0], 0);
         }
-    } else if (warp >= 10) {
+    } else if (warp == 11) {
+        regs_decrease<80>();
+        if (lane == 0) {
+            // dQ += dS(n) K(n) (K in stage n % 3), dS from TMEM slot n % 2: K-steps of 16
+            // keys, keys 64 c .. 64 c + 63 packed at slot + 32 c
+            constexpr uint32_t kIdG = idesc_bf16_f32(128, D, false, true);
+            int n = 0;
+            bool ok = true;
+            for (int j = lo; ok && j < hi; ++j, ++n) {
+                const int sk = n % kKStages;
+                ok = wd.wait(&bars->p_full[n & 1], (n >> 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t k_base = smem_u32(sK + sk * C::kTile);
+                const uint32_t slot = kColDS + 64 * (n & 1);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    umma_ts(tmem + kColDQ, tmem + slot + 32 * (kk >> 2) + 8 * (kk & 3),
+                            sdesc_sw128(k_base + kk * 2048, C::kAtom, 1024), kIdG,
+                            (n > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&bars->p_empty[n & 1]);
+                umma_commit(&bars->in_empty[sk]);
+            }
+            umma_commit(&bars->mm_done);
+            umma_commit(&bars->drain[1]);
+            bwd_drain(&bars->drain[1], 0);
+        }
+    } else if (warp == 10) {
         regs_decrease<80>();
     } else {
         regs_increase<208>();
