@@ -241,11 +241,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     const int j = blockIdx.x;  // key block
     if (j * 128 >= sq.Lk) return;
     const int n_qt = (sq.Lq + p.tpt - 1) / p.tpt;
-    auto tok_hi = [&](int i) { return min(i * p.tpt + p.tpt, sq.Lq) - 1; };
+    // (the lambdas take copies: a reference to the parameter block would turn each use into a
+    // load through a generic pointer)
+    const int tpt = p.tpt, causal = p.causal, wl = p.wl, wr = p.wr, Lq = sq.Lq, Lk = sq.Lk;
+    auto tok_hi = [=](int i) { return min(i * tpt + tpt, Lq) - 1; };
     // Does Q tile i see key block j?  (the forward pass's block range, per tile)
-    auto sees = [&](int i) {
-        const KvRange r = kv_block_range(i * p.tpt, tok_hi(i), sq.Lq, sq.Lk, 128, p.causal, p.wl,
-                                         p.wr);
+    auto sees = [=](int i) {
+        const KvRange r = kv_block_range(i * tpt, min(i * tpt + tpt, Lq) - 1, Lq, Lk, 128, causal,
+                                         wl, wr);
         return r.lo <= j && j < r.hi;
     };
 
