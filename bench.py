@@ -175,14 +175,17 @@ def oracle_rate(case, seconds, seed=0):
         lo = 0 if case.window_left < 0 else max(0, i - case.window_left)
         return max(0, hi - lo + 1)
 
-    # calibrate on a small sample, then run a sample sized for `seconds`
-    t, h = rows(32)
-    t0 = time.perf_counter()
-    oracle.attn_fwd_rows(case.q, case.k, case.v, case.cu_seqlens_q, case.cu_seqlens_k,
-                         case.softmax_scale, t, h, case.causal, case.window_left,
-                         case.window_right)
-    dt = max(time.perf_counter() - t0, 1e-4)
-    n = int(max(32, min(200000, 32 * seconds / dt)))
+    # calibrate on a small sample and then on one of about a second (fixed costs dominate the
+    # first), then run a sample sized for `seconds`
+    n = 32
+    for target in (1.0, seconds):
+        t, h = rows(n)
+        t0 = time.perf_counter()
+        oracle.attn_fwd_rows(case.q, case.k, case.v, case.cu_seqlens_q, case.cu_seqlens_k,
+                             case.softmax_scale, t, h, case.causal, case.window_left,
+                             case.window_right)
+        dt = max(time.perf_counter() - t0, 1e-4)
+        n = int(max(32, min(2000000, n * target / dt)))
     t, h = rows(n)
     t0 = time.perf_counter()
     oracle.attn_fwd_rows(case.q, case.k, case.v, case.cu_seqlens_q, case.cu_seqlens_k,
