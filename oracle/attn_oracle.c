@@ -676,3 +676,42 @@ int oracle_num_threads(void) {
     return 1;
 #endif
 }
+
+/* ---- FP8 (e4m3) inputs ------------------------------------------------------------------- */
+
+/*
+ * "Attention kernels: FlashAttention and PagedAttention", section 四.2 (FlashAttention-3): the
+ * FP8 forward feeds Q, K and V to the 8-bit MMA as e4m3 values with block-wise scales.  The
+ * e4m3 format itself is the standard 8-bit float (OCP 8-bit floating point, E4M3): a sign bit,
+ * 4 exponent bits with bias 7 and 3 mantissa bits; exponent field 0 holds the subnormals
+ * (m / 8) 2^-6; exponent field 15 with mantissa 7 is NaN; there is no infinity, so the largest
+ * finite magnitude is 1.75 * 2^8 = 448.
+ */
+double oracle_e4m3_to_f64(int code) {
+    const int s = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double v = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/*
+ * The e4m3 code nearest to x, ties to the code with the even mantissa, with magnitudes beyond
+ * 448 saturated to 448 (a saturating conversion); NaN gives 0x7F.  A plain search over the
+ * 127 non-negative finite codes, whose values increase with the code.
+ */
+int oracle_f64_to_e4m3(double x) {
+    if (isnan(x)) return 0x7F;
+    const int sign = signbit(x) ? 0x80 : 0;
+    const double a = fabs(x);
+    if (a >= 448.0) return sign | 0x7E;
+    int best = 0;
+    double best_d = a;  /* distance to code 0 (value 0) */
+    for (int c = 1; c <= 0x7E; ++c) {
+        const double d = fabs(a - oracle_e4m3_to_f64(c));
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return sign | best;
+}

@@ -83,6 +83,10 @@ def _load():
                                             i32, i32, P, P, P, P]
             lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
             lib.oracle_f64_to_bf16.argtypes = [dbl]
+            lib.oracle_e4m3_to_f64.restype = dbl
+            lib.oracle_e4m3_to_f64.argtypes = [i32]
+            lib.oracle_f64_to_e4m3.restype = i32
+            lib.oracle_f64_to_e4m3.argtypes = [dbl]
             lib.oracle_kvcache_prefill.restype = i32
             lib.oracle_kvcache_prefill.argtypes = [P, P, P, i32, P, P, P, P, i32, i32, i32, P,
                                                    i32, i32, i32, i32, P, P, i32, i32, i32, dbl,
@@ -364,3 +368,85 @@ def tiled_traffic_bytes(N, d, Br) -> int:
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+# ---- FP8 (e4m3) forward ------------------------------------------------------------------
+#
+# "Attention kernels: FlashAttention and PagedAttention", section 四.2 (FlashAttention-3): Q, K
+# and V go to the 8-bit MMA as e4m3 with block-wise scales, and V is re-laid out so that the
+# PV product reads it key-major.  The oracle decodes the codes (the e4m3 definition above),
+# applies the scales and runs the plain fp64 attention on the values; the e4m3 rounding of P
+# inside the FP8 kernel is an approximation of that result, bounded in the design notes.
+#
+# Scale and layout reading (the page fixes neither):
+#   q_scale [Hq, ceil(total_q / 128)]   one scale per 128 consecutive packed query tokens;
+#   k_scale [Hkv, nkb]                  one scale per 128-key block of a sequence
+#                                       (block kb0[b] + (t - k0) // 128);
+#   v8t     [Hkv, d, 128 * nkb]         V transposed, key t of sequence b in column
+#                                       128 * kb0[b] + (t - k0); the rest is padding;
+#   v_scale [batch, Hkv]                one scale per (sequence, kv head);
+# with kb0 the exclusive prefix sum of ceil(Lk_b / 128) and nkb >= kb0[batch].
+
+def e4m3_to_f64(codes):
+    """Decode e4m3 codes (any integer array) to fp64."""
+    lut = np.array([_load().oracle_e4m3_to_f64(c) for c in range(256)], np.float64)
+    return lut[np.asarray(codes, dtype=np.int64) & 0xFF]
+
+
+def f64_to_e4m3(x) -> int:
+    """Nearest e4m3 code of x (ties to even, saturating at 448)."""
+    return int(_load().oracle_f64_to_e4m3(float(x)))
+
+
+def key_block_offsets(cu_seqlens_k):
+    """kb0: exclusive prefix sum of ceil(Lk_b / 128) (length batch + 1)."""
+    cu = _i32(cu_seqlens_k).astype(np.int64)
+    nb = (cu[1:] - cu[:-1] + 127) // 128
+    return np.concatenate([[0], np.cumsum(nb)]).astype(np.int64)
+
+
+def fp8_dequantize(q8, k8, v8t, q_scale, k_scale, v_scale, cu_seqlens_k):
+    """fp64 Q [total_q, Hq, d], K, V [total_k, Hkv, d] from the FP8 inputs and their scales."""
+    def arr(x):
+        try:
+            import torch
+            if isinstance(x, torch.Tensor):
+                x = x.detach().cpu()
+                if x.dtype == torch.uint8:
+                    return x.numpy()
+                return x.double().numpy()
+        except ImportError:  # pragma: no cover
+            pass
+        return np.asarray(x)
+    q8, k8, v8t = arr(q8), arr(k8), arr(v8t)
+    qs, ks, vs = (arr(x).astype(np.float64) for x in (q_scale, k_scale, v_scale))
+    total_q, Hq, d = q8.shape
+    total_k, Hkv, _ = k8.shape
+    cu = _i32(cu_seqlens_k).astype(np.int64)
+    kb0 = key_block_offsets(cu)
+    q = e4m3_to_f64(q8) * qs.T[np.arange(total_q) // 128][:, :, None]
+    k = e4m3_to_f64(k8)
+    v = np.zeros((total_k, Hkv, d), np.float64)
+    vt = e4m3_to_f64(v8t)
+    for b in range(len(cu) - 1):
+        k0, k1 = int(cu[b]), int(cu[b + 1])
+        if k1 == k0:
+            continue
+        t = np.arange(k0, k1)
+        blk = kb0[b] + (t - k0) // 128
+        k[k0:k1] *= ks.T[blk][:, :, None]
+        cols = 128 * kb0[b] + (t - k0)
+        v[k0:k1] = vt[:, :, cols].transpose(2, 0, 1) * vs[b][None, :, None]
+    return q, k, v
+
+
+def fp8_attn_fwd(q8, k8, v8t, q_scale, k_scale, v_scale, cu_seqlens_q, cu_seqlens_k,
+                 softmax_scale, causal=False, window_left=-1, window_right=-1, rows=None):
+    """Attention on the dequantized FP8 inputs: every row (out [total_q, Hq, d], lse [Hq,
+    total_q]) or, with rows = (tok, head), the chosen rows (out [n, d], lse [n])."""
+    q, k, v = fp8_dequantize(q8, k8, v8t, q_scale, k_scale, v_scale, cu_seqlens_k)
+    if rows is None:
+        return attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, softmax_scale, causal,
+                        window_left, window_right)
+    return attn_fwd_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, softmax_scale, rows[0], rows[1],
+                         causal, window_left, window_right)
