@@ -63,6 +63,8 @@ def load():
             lib.attn_fwd_kvcache.argtypes = [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, P, P,
                                              i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                              ctypes.c_float, i32, i32, i32, P, sz, P]
+            lib.attn_fwd_fp8.restype = i32
+            lib.attn_fwd_fp8.argtypes = [P] * 10 + [i32] * 9 + [f32, i32, i32, i32, P]
             lib.attn_fwd_mods.restype = i32
             lib.attn_fwd_mods.argtypes = [P, P, P, P, P, P, P] + [i32] * 8 + [f32, i32, i32, i32,
                                                                             f32, P, P, sz, P]
@@ -221,6 +223,38 @@ def attn_fwd_mods(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_
                            _ptr(alibi_slopes), _ptr(ws), nbytes, _stream(stream))
     if rc != 0:
         raise AttnError(rc, "attn_fwd_mods")
+    return out, lse
+
+
+def attn_fwd_fp8(q8, k8, v8t, q_scale, k_scale, v_scale, cu_seqlens_q, cu_seqlens_k,
+                 max_seqlen_q, max_seqlen_k, softmax_scale=None, causal=False, window_left=-1,
+                 window_right=-1, out=None, lse=None, stream=None):
+    """FP8 (e4m3) forward.  q8 [total_q, Hq, 128], k8 [total_k, Hkv, 128] and v8t [Hkv, 128,
+    128 * key_blocks] are uint8 e4m3 codes; q_scale [Hq, ceil(total_q/128)], k_scale [Hkv,
+    key_blocks], v_scale [batch, Hkv] fp32.  Returns (out bf16, lse fp32) as attn_fwd."""
+    lib = load()
+    _check(q8, "q8", torch.uint8, 3)
+    _check(k8, "k8", torch.uint8, 3)
+    _check(v8t, "v8t", torch.uint8, 3)
+    _check(q_scale, "q_scale", torch.float32, 2)
+    _check(k_scale, "k_scale", torch.float32, 2)
+    _check(v_scale, "v_scale", torch.float32, 2)
+    total_q, Hq, d = q8.shape
+    total_k, Hkv, _ = k8.shape
+    key_blocks = k_scale.shape[1]
+    if v8t.shape != (Hkv, d, 128 * key_blocks):
+        raise ValueError("v8t must be [Hkv, d, 128 * key_blocks]")
+    batch = cu_seqlens_q.numel() - 1
+    scale = d ** -0.5 if softmax_scale is None else float(softmax_scale)
+    out = torch.empty((total_q, Hq, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
+    lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q8.device) if lse is None else lse
+    rc = lib.attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8t), _ptr(q_scale), _ptr(k_scale),
+                          _ptr(v_scale), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q),
+                          _ptr(cu_seqlens_k), batch, total_q, total_k, int(max_seqlen_q),
+                          int(max_seqlen_k), Hq, Hkv, d, key_blocks, scale, int(bool(causal)),
+                          int(window_left), int(window_right), _stream(stream))
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd_fp8")
     return out, lse
 
 

@@ -74,6 +74,20 @@ attn_status_t encode_3d(CUtensorMap* map, const void* base, uint64_t n0, uint64_
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// 3-D byte tensor [n2][n1][n0] (n0 innermost), box {b0, b1, b2}, 128-byte swizzle.
+attn_status_t encode_3d_u8(CUtensorMap* map, const void* base, uint64_t n0, uint64_t n1,
+                           uint64_t n2, uint32_t b0, uint32_t b1, uint32_t b2) {
+    const cuuint64_t dims[3] = {n0, n1, n2};
+    const cuuint64_t strides[2] = {n0, n0 * n1};
+    const cuuint32_t box[3] = {b0, b1, b2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Work items (pairs of 128-row Q tiles) the prefill list can hold.
@@ -262,6 +276,73 @@ attn_status_t attn_fwd_mods(const void* q, const void* k, const void* v, void* o
                     max_seqlen_q, max_seqlen_k, nheads_q, nheads_kv, head_dim, softmax_scale,
                     causal, window_left, window_right, workspace, workspace_bytes, stream,
                     softcap, alibi_slopes);
+}
+
+attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
+                           const float* q_scale, const float* k_scale, const float* v_scale,
+                           void* out, float* lse, const int32_t* cu_seqlens_q,
+                           const int32_t* cu_seqlens_k, int batch, int total_q, int total_k,
+                           int max_seqlen_q, int max_seqlen_k, int nheads_q, int nheads_kv,
+                           int head_dim, int key_blocks, float softmax_scale, int causal,
+                           int window_left, int window_right, void* stream) {
+    if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
+        nheads_q <= 0 || nheads_kv <= 0 || key_blocks < 0 || window_left < -1 ||
+        window_right < -1 || !scale_ok(softmax_scale))
+        return ATTN_ERR_INVALID_ARG;
+    if (nheads_q % nheads_kv != 0) return ATTN_ERR_INVALID_ARG;
+    if (head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+    const int g = nheads_q / nheads_kv;
+    if (g > 128) return ATTN_ERR_UNSUPPORTED;
+    if (batch == 0 || total_q == 0) return ATTN_OK;
+    if (!q8 || !k8 || !v8t || !q_scale || !k_scale || !v_scale || !out || !lse ||
+        !cu_seqlens_q || !cu_seqlens_k || key_blocks == 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (!aligned(q8, 16) || !aligned(k8, 16) || !aligned(v8t, 16) || !aligned(out, 16) ||
+        !aligned(q_scale, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4) || !aligned(lse, 4) ||
+        !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4))
+        return ATTN_ERR_INVALID_ARG;
+    if (static_cast<long long>(total_q) * nheads_q > (1LL << 31) - 1 ||
+        static_cast<long long>(total_k) * nheads_kv > (1LL << 31) - 1 ||
+        static_cast<long long>(key_blocks) * 128 * head_dim * nheads_kv > (1LL << 40) ||
+        static_cast<long long>(batch) * nheads_kv > 65535)
+        return ATTN_ERR_UNSUPPORTED;
+
+    DeviceState* dev = nullptr;
+    attn_status_t st = device_state(&dev);
+    if (st != ATTN_OK) return st;
+
+    const int tpt = tokens_per_tile(g);
+    Fp8Params fp;
+    memset(&fp, 0, sizeof(fp));
+    if (encode_3d_u8(&fp.tm_q, q8, head_dim, nheads_q, total_q, 128, g, tpt) != ATTN_OK ||
+        encode_3d_u8(&fp.tm_k, k8, head_dim, nheads_kv, total_k > 0 ? total_k : 1, 128, 1, 128) != ATTN_OK ||
+        encode_3d_u8(&fp.tm_v, v8t, 128ull * key_blocks, head_dim, nheads_kv, 128, 128, 1) != ATTN_OK)
+        return ATTN_ERR_CUDA;
+    fp.q_scale = q_scale;
+    fp.k_scale = k_scale;
+    fp.v_scale = v_scale;
+    fp.out = static_cast<__nv_bfloat16*>(out);
+    fp.lse = lse;
+    fp.cu_q = cu_seqlens_q;
+    fp.cu_k = cu_seqlens_k;
+    fp.status = dev->status;
+    fp.batch = batch;
+    fp.Hq = nheads_q;
+    fp.Hkv = nheads_kv;
+    fp.g = g;
+    fp.tpt = tpt;
+    fp.total_q = total_q;
+    fp.total_k = total_k;
+    fp.max_seqlen_q = max_seqlen_q;
+    fp.max_seqlen_k = max_seqlen_k;
+    fp.nqb = (total_q + 127) / 128;
+    fp.nkb = key_blocks;
+    fp.causal = causal ? 1 : 0;
+    fp.wl = window_left;
+    fp.wr = window_right;
+    fp.scale_log2 = softmax_scale * kLog2eF;
+    if (launch_fwd_fp8(fp, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
 }
 
 size_t attn_fwd_kvcache_workspace_bytes(int batch, int total_q, int max_seqlen_q, int nheads_q,

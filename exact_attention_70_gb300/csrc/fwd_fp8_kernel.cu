@@ -1,0 +1,358 @@
+// fwd_fp8_kernel.cu -- FP8 (e4m3) forward pass of exact attention on tcgen05 tensor cores.
+//
+// The method ("Attention kernels: FlashAttention and PagedAttention", section 四.2,
+// FlashAttention-3): Q, K and V go to the 8-bit MMA as e4m3 values with block-wise scales, and
+// V is re-laid out so that the P V product reads it key-major.  Around the two products the
+// tiled online softmax is the one of the bf16 path (same page, section 三; "04 · FA4
+// (CuTeDSL) and engineering interfaces", sections 4-5 for varlen and GQA packing): a running
+// row maximum m and sum l, P~ = exp2(x - m), O rescaled when m moves.
+//
+// GB300 mapping: one CTA per 128-row packed Q tile (tokens x the g query heads of a kv head),
+// 192 threads:
+//   warps 0-3: the softmax, one thread per row (TMEM lane quarter = warp).  S of a key block is
+//              pulled into registers whole, so its TMEM buffer is free again at once; P goes to
+//              shared memory as e4m3 bytes of 16 P~ (P~ <= 2^4 with the lazy rescale below, so
+//              16 P~ <= 256 stays inside e4m3's range and its normal grid covers P~ >= 2^-10);
+//   warp 4:    TMA of the Q tile (once) and of K and V^T blocks into three-stage rings;
+//   warp 5:    the MMA issuer: S(n) = Q K(n)^T into TMEM buffer n % 2 (kind::f8f6f4, K = 32 per
+//              instruction), then O += P(n-1) V(n-1) (A = P from shared memory, B = the V^T
+//              block, both K-major), so S of the next block overlaps the softmax of this one.
+// Scales: S = (Q8 K8^T) q_scale[row] k_scale[block] enters the softmax as one multiplier per row
+// and block; v_scale (per sequence and kv head) multiplies O at the end, together with 1 / l.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tile_math.h"
+
+namespace attn {
+
+namespace {
+
+constexpr int kF8Threads = 192;
+constexpr int kF8Stages = 3;
+constexpr int kAtom = 128 * 128;      // 128 rows x 128 bytes, 128-byte swizzle
+constexpr float kPLog2 = 4.f;         // P is stored as 2^4 P~
+constexpr float kLazyLog2 = 4.f;      // O and l are rescaled only when m grows by more than this
+
+struct F8Bars {
+    uint64_t q_full;
+    uint64_t k_full[kF8Stages], k_empty[kF8Stages];
+    uint64_t v_full[kF8Stages], v_empty[kF8Stages];
+    uint64_t s_full[2], s_free[2];
+    uint64_t p_full[2], p_empty[2];
+    uint64_t pv_done, o_done, drain;
+    uint32_t tmem_base;
+    int kb0;
+    int abort_flag;
+};
+
+// Shared memory: Q tile, K ring, V^T ring, two P buffers (each one atom), barriers.
+constexpr int kOffQ = 0;
+constexpr int kOffK = kAtom;
+constexpr int kOffV = kOffK + kF8Stages * kAtom;
+constexpr int kOffP = kOffV + kF8Stages * kAtom;
+constexpr int kOffBars = kOffP + 2 * kAtom;
+constexpr int kF8Smem = kOffBars + static_cast<int>(sizeof(F8Bars)) + 1024;
+static_assert(kF8Smem <= 227 * 1024, "FP8 forward shared memory");
+
+__device__ void f8_drain(uint64_t* bar, uint32_t parity) {
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try(bar, parity))
+        if (global_ns() - t0 > 200000000ull) return;
+}
+
+__global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_constant__ Fp8Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    F8Bars* bars = reinterpret_cast<F8Bars*>(smem + kOffBars);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int b = blockIdx.y / p.Hkv, kvh = blockIdx.y % p.Hkv;
+    const int q0 = p.cu_q[b], Lq = p.cu_q[b + 1] - q0;
+    const int k0 = p.cu_k[b], Lk = p.cu_k[b + 1] - k0;
+    if (q0 < 0 || Lq < 0 || q0 + Lq > p.total_q || Lq > p.max_seqlen_q || k0 < 0 || Lk < 0 ||
+        k0 + Lk > p.total_k || Lk > p.max_seqlen_k) {
+        if (threadIdx.x == 0) atomicOr(p.status, kStatusBounds);
+        return;
+    }
+    const int i = gridDim.x - 1 - blockIdx.x;  // the tiles that see the most keys go first
+    if (i * p.tpt >= Lq) return;
+    const int imin = i * p.tpt, imax = min(imin + p.tpt, Lq) - 1;
+    const KvRange kr_ = kv_block_range(imin, imax, Lq, Lk, 128, p.causal, p.wl, p.wr);
+    const int lo = kr_.lo, hi = kr_.hi;
+
+    if (threadIdx.x == 0) {
+        // first 128-key block of this sequence in the V^T columns and the k_scale rows
+        int kb0 = 0;
+        for (int s = 0; s < b; ++s) kb0 += (p.cu_k[s + 1] - p.cu_k[s] + 127) / 128;
+        bars->kb0 = kb0;
+        mbar_init(&bars->q_full, 1);
+        for (int s = 0; s < kF8Stages; ++s) {
+            mbar_init(&bars->k_full[s], 1);
+            mbar_init(&bars->k_empty[s], 1);
+            mbar_init(&bars->v_full[s], 1);
+            mbar_init(&bars->v_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->s_full[s], 1);
+            mbar_init(&bars->s_free[s], 4);
+            mbar_init(&bars->p_full[s], 4);
+            mbar_init(&bars->p_empty[s], 1);
+        }
+        mbar_init(&bars->pv_done, 1);
+        mbar_init(&bars->o_done, 1);
+        mbar_init(&bars->drain, 1);
+        bars->abort_flag = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+    const int kb0 = bars->kb0;
+    if (kb0 + (Lk + 127) / 128 > p.nkb) {  // the scale and V^T tables are too short
+        if (threadIdx.x == 0) atomicOr(p.status, kStatusBounds);
+        return;
+    }
+    if (warp == 5) tmem_alloc(&bars->tmem_base, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    const Watchdog wd{&bars->abort_flag, p.status};
+    constexpr uint32_t kColO = 256;  // S buffers at columns 0 and 128
+
+    if (warp == 4) {
+        if (lane == 0 && hi > lo) {
+            tma_prefetch_desc(&p.tm_k);
+            tma_prefetch_desc(&p.tm_v);
+            mbar_arrive_expect_tx(&bars->q_full, 128u * p.g * p.tpt);
+            tma_load_3d(smem + kOffQ, &p.tm_q, &bars->q_full, 0, kvh * p.g, q0 + imin);
+            int nk = 0, nv = 0;
+            for (int j = lo; j < hi; ++j) {
+                const int sk = nk % kF8Stages;
+                if (nk >= kF8Stages && !wd.wait(&bars->k_empty[sk], ((nk / kF8Stages) - 1) & 1)) break;
+                mbar_arrive_expect_tx(&bars->k_full[sk], kAtom);
+                tma_load_3d(smem + kOffK + sk * kAtom, &p.tm_k, &bars->k_full[sk], 0, kvh,
+                            k0 + j * 128);
+                ++nk;
+                const int sv = nv % kF8Stages;
+                if (nv >= kF8Stages && !wd.wait(&bars->v_empty[sv], ((nv / kF8Stages) - 1) & 1)) break;
+                mbar_arrive_expect_tx(&bars->v_full[sv], kAtom);
+                tma_load_3d(smem + kOffV + sv * kAtom, &p.tm_v, &bars->v_full[sv], 128 * (kb0 + j),
+                            0, kvh);
+                ++nv;
+            }
+            f8_drain(&bars->q_full, 0);
+            for (int m = nk > kF8Stages ? nk - kF8Stages : 0; m < nk; ++m)
+                f8_drain(&bars->k_full[m % kF8Stages], (m / kF8Stages) & 1);
+            for (int m = nv > kF8Stages ? nv - kF8Stages : 0; m < nv; ++m)
+                f8_drain(&bars->v_full[m % kF8Stages], (m / kF8Stages) & 1);
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {
+            constexpr uint32_t kId = idesc_e4m3_f32(128, 128);
+            const uint64_t qd = sdesc_sw128(smem_u32(smem + kOffQ), 16, 1024);
+            // O += P(m) V(m): K-steps of 32 keys (32 bytes) along both K-major operands
+            auto pv = [&](int m) {
+                const int sv = m % kF8Stages, bm = m & 1;
+                if (!wd.wait(&bars->p_full[bm], (m >> 1) & 1) ||
+                    !wd.wait(&bars->v_full[sv], (m / kF8Stages) & 1))
+                    return false;
+                tc_fence_after();
+                const uint64_t pd = sdesc_sw128(smem_u32(smem + kOffP + bm * kAtom), 16, 1024);
+                const uint64_t vd = sdesc_sw128(smem_u32(smem + kOffV + sv * kAtom), 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_ss_f8(tmem + kColO, pd + 2 * kk, vd + 2 * kk, kId, (m > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&bars->p_empty[bm]);
+                umma_commit(&bars->v_empty[sv]);
+                umma_commit(&bars->pv_done);
+                return true;
+            };
+            int n = 0;
+            bool ok = hi > lo && wd.wait(&bars->q_full, 0);
+            for (int j = lo; ok && j < hi; ++j) {
+                const int sk = n % kF8Stages, bn = n & 1;
+                ok = wd.wait(&bars->k_full[sk], (n / kF8Stages) & 1) &&
+                     (n < 2 || wd.wait(&bars->s_free[bn], ((n - 2) >> 1) & 1));
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t kd = sdesc_sw128(smem_u32(smem + kOffK + sk * kAtom), 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_ss_f8(tmem + 128 * bn, qd + 2 * kk, kd + 2 * kk, kId, kk > 0 ? 1u : 0u);
+                umma_commit(&bars->s_full[bn]);
+                umma_commit(&bars->k_empty[sk]);
+                if (n >= 1 && !pv(n - 1)) {
+                    ok = false;
+                    break;
+                }
+                ++n;
+            }
+            if (ok && n >= 1) pv(n - 1);
+            umma_commit(&bars->o_done);
+            umma_commit(&bars->drain);
+            f8_drain(&bars->drain, 0);
+        }
+    } else {
+        // softmax: thread = packed row r of the tile
+        const int r = threadIdx.x;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+        const int tok = imin + r / p.g, head = kvh * p.g + r % p.g;
+        const bool valid = r < p.g * p.tpt && tok < Lq;
+        int kmin = 1, kmax = 0;
+        float qs = 0.f;
+        if (valid) {
+            row_key_interval(tok, Lq, Lk, p.causal, p.wl, p.wr, kmin, kmax);
+            qs = p.q_scale[static_cast<size_t>(head) * p.nqb + (q0 + tok) / 128];
+        }
+        const float* ks_row = p.k_scale + static_cast<size_t>(kvh) * p.nkb + kb0;
+        // this thread's row of the P buffers: 128 keys as bytes, 16-byte chunk c at c ^ (r % 8)
+        const uint32_t row_p = smem_u32(smem + kOffP) + r * 128;
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        int n = 0;
+        for (int j = lo; j < hi; ++j, ++n) {
+            const int bn = n & 1;
+            const bool masked = !valid || kv_block_masked(j, imin, imax, Lq, Lk, 128, p.causal,
+                                                          p.wl, p.wr);
+            // (kept positive so that a masked -inf never meets a zero multiplier)
+            const float c = fmaxf(qs * ks_row[j] * p.scale_log2, 1.17549435e-38f);
+            ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->s_full[bn], (n >> 1) & 1));
+            tc_fence_after();
+            uint32_t s[128];
+            if (ok) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    tmem_ld32(tmem + lane_off + 128 * bn + 32 * q,
+                              *reinterpret_cast<uint32_t(*)[32]>(s + 32 * q));
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int e = 0; e < 128; ++e) s[e] = 0u;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->s_free[bn]);
+            if (masked) {
+#pragma unroll
+                for (int e = 0; e < 128; ++e) {
+                    const int key = j * 128 + e;
+                    if (!valid || key < kmin || key > kmax) s[e] = __float_as_uint(-INFINITY);
+                }
+            }
+            // row maximum of the raw scores (c > 0 keeps the order)
+            float mx = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < 128; e += 2)
+                mx = fmax3(mx, __uint_as_float(s[e]), __uint_as_float(s[e + 1]));
+            const float xm = mx == -INFINITY ? -INFINITY : mx * c;
+            // lazy rescale: move m only when the block's maximum exceeds it by > 2^4
+            const bool grow = xm > m_used + kLazyLog2;
+            float alpha = 1.f;
+            if (grow) {
+                if (m_used != -INFINITY) alpha = exp2f(m_used - xm);
+                l *= alpha;
+                m_used = xm;
+            }
+            if (__any_sync(0xffffffffu, grow && alpha != 1.f) && n > 0) {
+                // O holds earlier blocks: wait for the last P V, then scale its rows
+                ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->pv_done, (n - 1) & 1));
+                tc_fence_after();
+                if (ok) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t o[32];
+                        tmem_ld32(tmem + lane_off + kColO + 32 * q, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(tmem + lane_off + kColO + 32 * q, o);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            // P = 2^4 exp2(x - m), x = s c; an empty row so far uses m = 0 (no -inf - -inf)
+            const float off = kPLog2 - (m_used == -INFINITY ? 0.f : m_used);
+            const uint64_t c2 = f2_make(c, c), off2 = f2_make(off, off);
+            uint32_t pk[32];
+            float sum = 0.f;
+#pragma unroll
+            for (int e = 0; e < 128; e += 4) {
+                float x0, x1, x2, x3;
+                f2_split(f2_fma(f2_make(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), c2, off2), x0, x1);
+                f2_split(f2_fma(f2_make(__uint_as_float(s[e + 2]), __uint_as_float(s[e + 3])), c2, off2), x2, x3);
+                x0 = ex2_approx(x0);
+                x1 = ex2_approx(x1);
+                x2 = ex2_approx(x2);
+                x3 = ex2_approx(x3);
+                sum += (x0 + x1) + (x2 + x3);
+                pk[e / 4] = pack_e4m3x4(x0, x1, x2, x3);
+            }
+            l += sum;
+            // buffer bn is free once P V of block n - 2 has read it
+            if (n >= 2)
+                ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->p_empty[bn], ((n - 2) >> 1) & 1));
+            if (ok) {
+                const uint32_t row = row_p + bn * kAtom;
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc)
+                    st_shared_v4(row + static_cast<uint32_t>(((cc ^ (r & 7)) * 16)), pk[4 * cc],
+                                 pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->p_full[bn]);
+        }
+        // Epilogue: O = v_scale O~ / l as bf16, LSE = ln 2 (m + log2 l - 4).
+        if (n > 0) {
+            ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->o_done, 0));
+            tc_fence_after();
+        }
+        const float vs = p.v_scale[static_cast<size_t>(b) * p.Hkv + kvh];
+        const float mul = l > 0.f ? vs / l : 0.f;
+        __nv_bfloat16* dst = p.out + (static_cast<size_t>(q0 + tok) * p.Hq + head) * 128;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t o[32];
+            if (n > 0 && ok) {
+                tmem_ld32(tmem + lane_off + kColO + 32 * q, o);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = 0u;
+            }
+            if (valid && ok) {
+                uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * q);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    d4[v] = make_uint4(
+                        pack_bf16x2(__uint_as_float(o[8 * v + 0]) * mul, __uint_as_float(o[8 * v + 1]) * mul),
+                        pack_bf16x2(__uint_as_float(o[8 * v + 2]) * mul, __uint_as_float(o[8 * v + 3]) * mul),
+                        pack_bf16x2(__uint_as_float(o[8 * v + 4]) * mul, __uint_as_float(o[8 * v + 5]) * mul),
+                        pack_bf16x2(__uint_as_float(o[8 * v + 6]) * mul, __uint_as_float(o[8 * v + 7]) * mul));
+            }
+        }
+        if (valid && ok)
+            p.lse[static_cast<size_t>(head) * p.total_q + q0 + tok] =
+                l > 0.f ? (m_used + log2f(l) - kPLog2) * 0.69314718055994531f : -INFINITY;
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_fp8(const Fp8Params& p, cudaStream_t stream) {
+    const dim3 grid((p.max_seqlen_q + p.tpt - 1) / p.tpt, p.batch * p.Hkv);
+    cudaFuncSetAttribute(fwd_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kF8Smem);
+    if (grid.x > 0 && grid.y > 0) fwd_fp8_kernel<<<grid, kF8Threads, kF8Smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -116,6 +116,31 @@ struct BwdParams {
 
 cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t stream);
 
+// ---- FP8 (e4m3) prefill ----------------------------------------------------------------
+
+// Scales: q_scale [Hq, nqb] per 128 consecutive packed query tokens; k_scale [Hkv, nkb] per
+// 128-key block of a sequence (block kb0[b] + (t - k0) / 128, kb0 the prefix sum of
+// ceil(Lk_b / 128)); v_scale [batch, Hkv].  V is stored transposed: v8t [Hkv, d, 128 nkb],
+// key t of sequence b in column 128 (kb0[b]) + (t - k0).
+struct Fp8Params {
+    CUtensorMap tm_q;   // 3-D over q8  [total_q, Hq, d] u8, box {d, g, tpt}
+    CUtensorMap tm_k;   // 3-D over k8  [total_k, Hkv, d] u8, box {d, 1, 128}
+    CUtensorMap tm_v;   // 3-D over v8t [Hkv, d, 128 nkb] u8, box {128, d, 1}
+    const float* q_scale;
+    const float* k_scale;
+    const float* v_scale;
+    __nv_bfloat16* out;
+    float* lse;
+    const int* cu_q;
+    const int* cu_k;
+    unsigned* status;
+    int batch, Hq, Hkv, g, tpt, total_q, total_k, max_seqlen_q, max_seqlen_k, nqb, nkb;
+    int causal, wl, wr;
+    float scale_log2;
+};
+
+cudaError_t launch_fwd_fp8(const Fp8Params& p, cudaStream_t stream);
+
 // ---- failure-path self-test ------------------------------------------------------------
 
 cudaError_t launch_watchdog_selftest(unsigned* status, cudaStream_t stream);

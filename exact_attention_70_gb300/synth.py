@@ -243,3 +243,92 @@ def chunked_case() -> KvcacheCase:
     ctx = torch.randint(2048, 16384 + 1, (8,), generator=g).tolist()
     return kvcache_case([2048] * 8, ctx, 32, 8, 128, 256, seed=1101, rotary_dim=128,
                         name="chunked")
+
+
+# ---- FP8 (e4m3) inputs -------------------------------------------------------------------
+#
+# Recipe: e4m3 bit patterns drawn directly (no rounding of values happens here): the sign bit
+# and the 3 mantissa bits uniform, the 4-bit exponent field uniform in [4, 10], i.e. magnitudes
+# log-uniform over [2^-3, 15]; the NaN pattern never occurs.  Scales are uniform in
+# [0.15, 0.25] (decoded values then have an RMS near 1).  V^T columns past a sequence's keys
+# (the layout's padding) are code 0 (value 0).
+
+def e4m3_codes(shape, seed: int, stream: int = 0) -> torch.Tensor:
+    """Random e4m3 bit patterns (uint8), reproducible for (shape, seed, stream)."""
+    numel = math.prod(shape)
+    out = torch.empty(numel, dtype=torch.uint8)
+    nblk = (numel + _BLOCK - 1) // _BLOCK
+
+    def fill(i):
+        s, e = i * _BLOCK, min(numel, (i + 1) * _BLOCK)
+        g = torch.Generator().manual_seed(seed * 1_000_003 + stream * 65_537 + i)
+        bits = torch.randint(0, 1 << 30, (e - s,), generator=g, dtype=torch.int64)
+        sign = (bits & 1) << 7
+        man = (bits >> 1) & 7
+        exp = 4 + (bits >> 4) % 7
+        out[s:e].copy_((sign | (exp << 3) | man).to(torch.uint8))
+
+    if nblk <= 2:
+        for i in range(nblk):
+            fill(i)
+    else:
+        with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, range(nblk)))
+    return out.view(*shape)
+
+
+@dataclass
+class Fp8Case:
+    name: str
+    q8: torch.Tensor        # uint8 [total_q, Hq, d]
+    k8: torch.Tensor        # uint8 [total_k, Hkv, d]
+    v8t: torch.Tensor       # uint8 [Hkv, d, 128 * key_blocks]
+    q_scale: torch.Tensor   # fp32 [Hq, ceil(total_q / 128)]
+    k_scale: torch.Tensor   # fp32 [Hkv, key_blocks]
+    v_scale: torch.Tensor   # fp32 [batch, Hkv]
+    cu_seqlens_q: torch.Tensor
+    cu_seqlens_k: torch.Tensor
+    max_seqlen_q: int
+    max_seqlen_k: int
+    softmax_scale: float
+    causal: bool
+    window_left: int = -1
+    window_right: int = -1
+
+
+def fp8_case(lengths_q, Hq, Hkv, d, causal, seed, lengths_k=None, window=(-1, -1), scale=None,
+             name="fp8") -> Fp8Case:
+    lengths_k = list(lengths_q) if lengths_k is None else list(lengths_k)
+    cu_q, cu_k = cu_from_lengths(lengths_q), cu_from_lengths(lengths_k)
+    tq, tk = int(cu_q[-1]), int(cu_k[-1])
+    blocks = [(int(n) + 127) // 128 for n in lengths_k]
+    key_blocks = max(1, sum(blocks))
+    v8t = e4m3_codes((Hkv, d, 128 * key_blocks), seed, 3)
+    col = 0
+    for n, nb in zip(lengths_k, blocks):   # zero the padding columns of each sequence
+        v8t[:, :, col + int(n):col + 128 * nb] = 0
+        col += 128 * nb
+    v8t[:, :, col:] = 0
+    g = torch.Generator().manual_seed(seed * 7 + 5)
+    return Fp8Case(
+        name=name,
+        q8=e4m3_codes((tq, Hq, d), seed, 1),
+        k8=e4m3_codes((tk, Hkv, d), seed, 2),
+        v8t=v8t,
+        q_scale=0.15 + 0.1 * torch.rand((Hq, (tq + 127) // 128), generator=g),
+        k_scale=0.15 + 0.1 * torch.rand((Hkv, key_blocks), generator=g),
+        v_scale=0.15 + 0.1 * torch.rand((len(lengths_q), Hkv), generator=g),
+        cu_seqlens_q=cu_q, cu_seqlens_k=cu_k,
+        max_seqlen_q=max([0] + [int(x) for x in lengths_q]),
+        max_seqlen_k=max([0] + [int(x) for x in lengths_k]),
+        softmax_scale=d ** -0.5 if scale is None else scale, causal=bool(causal),
+        window_left=window[0], window_right=window[1],
+    )
+
+
+FP8_NAME = "FP8 e4m3 causal prefill B=4 Hq=Hkv=16 N=4096 d=128"
+
+
+def fp8_bench_case() -> Fp8Case:
+    """The causal prefill workload's shape with FP8 inputs."""
+    return fp8_case([4096] * 4, 16, 16, 128, True, seed=1200, name="fp8")

@@ -240,6 +240,33 @@ attn_status_t attn_fwd_mods(const void* q, const void* k, const void* v, void* o
                             const float* alibi_slopes, void* workspace, size_t workspace_bytes,
                             void* stream);
 
+/*
+ * FP8 (e4m3) forward ("Attention kernels: FlashAttention and PagedAttention", section 四.2,
+ * FlashAttention-3): Q, K and V as e4m3 bytes with block-wise fp32 scales, V re-laid out
+ * key-major; the result is the attention of the dequantized values.
+ *   q8      device u8 e4m3 [total_q, nheads_q, head_dim]
+ *   k8      device u8 e4m3 [total_k, nheads_kv, head_dim]
+ *   v8t     device u8 e4m3 [nheads_kv, head_dim, 128 * key_blocks]: V transposed; key t of
+ *           sequence b sits in column 128 * kb0[b] + (t - cu_seqlens_k[b]), kb0 the prefix sum
+ *           of ceil(Lk_b / 128); columns past a sequence's keys must hold finite values (zero)
+ *   q_scale device fp32 [nheads_q, ceil(total_q / 128)]: one scale per 128 consecutive packed
+ *           query tokens (row value = code * scale)
+ *   k_scale device fp32 [nheads_kv, key_blocks]: one scale per 128-key block of a sequence
+ *           (block kb0[b] + (t - cu_seqlens_k[b]) / 128)
+ *   v_scale device fp32 [batch, nheads_kv]: one scale per (sequence, kv head)
+ *   key_blocks >= kb0[batch]; a sequence whose blocks run past it sets the device bounds flag.
+ * out, lse, cu_seqlens, sizes, causal and window as attn_fwd; head_dim must be 128.  Within
+ * the kernel P is rounded to e4m3 (as 16 P~ with P~ <= 16, see the design notes for the bound
+ * on O), S and O accumulate in fp32, and LSE is computed from the unrounded P~.
+ */
+attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
+                           const float* q_scale, const float* k_scale, const float* v_scale,
+                           void* out, float* lse, const int32_t* cu_seqlens_q,
+                           const int32_t* cu_seqlens_k, int batch, int total_q, int total_k,
+                           int max_seqlen_q, int max_seqlen_k, int nheads_q, int nheads_kv,
+                           int head_dim, int key_blocks, float softmax_scale, int causal,
+                           int window_left, int window_right, void* stream);
+
 /* Bytes of split-partial workspace for attn_decode_kvcache; num_splits 0 sizes for the
  * automatic choice (at most 16 splits).  0 when one split needs no workspace. */
 size_t attn_decode_workspace_bytes(int batch, int nheads_q, int head_dim, int num_splits);

@@ -1,0 +1,97 @@
+"""FP8 (e4m3) forward against the oracle on the dequantized inputs.
+
+Tolerance (derived in the design notes from the e4m3 grid): P is rounded to e4m3 inside the
+kernel, each element to within 2^-4 of itself (normal range; 16 P~ <= 256 keeps it there for
+P~ >= 2^-10), so |O - O_ref| <= 2^-4 max|V| per element, plus bf16 rounding of O (2^-8 |O|);
+the mean error is far below that because the roundings do not add up coherently, and the test
+bounds it by 2^-7 mean|V|.  LSE comes from the unrounded P~: 1e-3."""
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_70_gb300 import binding, synth
+from oracle import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def run(c):
+    dev = "cuda"
+    out, lse = binding.attn_fwd_fp8(c.q8.to(dev), c.k8.to(dev), c.v8t.to(dev),
+                                    c.q_scale.to(dev), c.k_scale.to(dev), c.v_scale.to(dev),
+                                    c.cu_seqlens_q.to(dev), c.cu_seqlens_k.to(dev),
+                                    c.max_seqlen_q, c.max_seqlen_k, c.softmax_scale, c.causal,
+                                    c.window_left, c.window_right)
+    torch.cuda.synchronize()
+    assert binding.attn_get_device_status() == 0
+    return out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def check(c, out, lse, ref_o, ref_l, vmax, vmean, rows=None):
+    if rows is not None:
+        out = out[rows[0], rows[1]]
+        lse = lse[rows[1], rows[0]]
+    err = np.abs(out - ref_o)
+    bound = 2.0 ** -4 * vmax + 2.0 ** -8 * np.abs(ref_o) + 1e-6
+    assert np.all(err <= bound), (err.max(), (err / bound).max())
+    assert err.mean() <= 2.0 ** -7 * vmean, (err.mean(), vmean)
+    fin = np.isfinite(ref_l)
+    assert np.array_equal(fin, np.isfinite(lse))
+    assert np.abs(lse[fin] - ref_l[fin]).max() <= 1e-3
+
+
+def v_stats(c):
+    _, _, v = oracle.fp8_dequantize(c.q8, c.k8, c.v8t, c.q_scale, c.k_scale, c.v_scale,
+                                    c.cu_seqlens_k)
+    return np.abs(v).max(), np.abs(v).mean()
+
+
+CASES = [
+    dict(lq=[256], Hq=2, Hkv=2, causal=True),
+    dict(lq=[5, 130, 300], Hq=8, Hkv=2, causal=True),
+    dict(lq=[100, 257], lk=[300, 64], Hq=4, Hkv=4, causal=False),
+    dict(lq=[400], Hq=4, Hkv=1, causal=True, window=(64, 0)),
+    dict(lq=[190, 77], Hq=4, Hkv=2, causal=False, window=(32, 16)),
+    dict(lq=[129, 0, 255], Hq=6, Hkv=2, causal=True),
+    dict(lq=[64, 200], lk=[500, 700], Hq=4, Hkv=2, causal=True),
+]
+
+
+@pytest.mark.parametrize("i", range(len(CASES)))
+def test_fp8_forward_matches_oracle(i):
+    k = CASES[i]
+    c = synth.fp8_case(k["lq"], k["Hq"], k["Hkv"], 128, k["causal"], seed=300 + i,
+                       lengths_k=k.get("lk"), window=k.get("window", (-1, -1)))
+    out, lse = run(c)
+    ref_o, ref_l = oracle.fp8_attn_fwd(c.q8, c.k8, c.v8t, c.q_scale, c.k_scale, c.v_scale,
+                                       c.cu_seqlens_q, c.cu_seqlens_k, c.softmax_scale,
+                                       c.causal, c.window_left, c.window_right)
+    vmax, vmean = v_stats(c)
+    check(c, out, lse, ref_o, ref_l, vmax, vmean)
+
+
+def test_fp8_forward_full_size_sampled_rows():
+    c = synth.fp8_bench_case()
+    out, lse = run(c)
+    g = torch.Generator().manual_seed(9)
+    n = 256
+    tok = torch.randint(0, c.q8.shape[0], (n,), generator=g).numpy()
+    head = torch.randint(0, c.q8.shape[1], (n,), generator=g).numpy()
+    tok[:4] = [0, 127, 128, 4095]
+    ref_o, ref_l = oracle.fp8_attn_fwd(c.q8, c.k8, c.v8t, c.q_scale, c.k_scale, c.v_scale,
+                                       c.cu_seqlens_q, c.cu_seqlens_k, c.softmax_scale,
+                                       c.causal, rows=(tok, head))
+    vmax, vmean = v_stats(c)
+    check(c, out, lse, ref_o, ref_l, vmax, vmean, rows=(tok, head))
+
+
+def test_fp8_short_key_tables_raise_the_bounds_flag():
+    c = synth.fp8_case([300], 2, 1, 128, True, seed=5)
+    dev = "cuda"
+    ks = c.k_scale[:, :2].contiguous()        # 300 keys need three blocks
+    vt = c.v8t[:, :, :256].contiguous()
+    binding.attn_fwd_fp8(c.q8.to(dev), c.k8.to(dev), vt.to(dev), c.q_scale.to(dev), ks.to(dev),
+                         c.v_scale.to(dev), c.cu_seqlens_q.to(dev), c.cu_seqlens_k.to(dev),
+                         c.max_seqlen_q, c.max_seqlen_k, c.softmax_scale, True)
+    torch.cuda.synchronize()
+    assert binding.attn_get_device_status() == -6      # ATTN_ERR_DEVICE_BOUNDS

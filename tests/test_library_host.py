@@ -223,3 +223,28 @@ def test_modifier_arguments_are_checked(lib):
     assert call(19, float("nan")) == -1
     assert call(20, P(4098)) == -1           # misaligned slopes
     assert call(7, 0) == 0                   # batch 0
+
+
+def test_fp8_arguments_are_checked(lib):
+    P = ctypes.c_void_p
+    fake = P(4096)
+    f = lib.attn_fwd_fp8
+    # q8 k8 v8t q_scale k_scale v_scale out lse cu_q cu_k | batch total_q total_k max_q max_k
+    # Hq Hkv d key_blocks | scale causal wl wr stream
+    base = [fake] * 10 + [1, 16, 16, 16, 16, 4, 2, 128, 1, 0.1, 1, -1, -1, None]
+
+    def call(i, v):
+        a = list(base)
+        a[i] = v
+        return f(*a)
+
+    assert call(17, 64) == -2               # head_dim 64 is not built for FP8
+    assert call(15, 5) == -1                # Hq % Hkv != 0
+    assert call(18, 0) == -1                # no key blocks
+    assert call(18, -1) == -1
+    assert call(19, -0.1) == -1             # scale
+    assert call(0, None) == -1              # null q8
+    assert call(1, P(4097)) == -1           # misaligned k8
+    assert call(3, P(4098)) == -1           # misaligned q_scale
+    assert call(21, -2) == -1               # window
+    assert call(10, 0) == 0                 # batch 0
