@@ -7,18 +7,19 @@
 // (CuTeDSL) and engineering interfaces", sections 4-5 for varlen and GQA packing): a running
 // row maximum m and sum l, P~ = exp2(x - m), O rescaled when m moves.
 //
-// GB300 mapping: one CTA per 128-row packed Q tile (tokens x the g query heads of a kv head),
-// 192 threads:
-//   warps 0-3: the softmax, one thread per row (TMEM lane quarter = warp).  S of a key block is
-//              pulled into registers whole, so its TMEM buffer is free again at once; P goes to
-//              shared memory as e4m3 bytes of 16 P~ (P~ <= 2^4 with the lazy rescale below, so
-//              16 P~ <= 256 stays inside e4m3's range and its normal grid covers P~ >= 2^-10);
-//   warp 4:    TMA of the Q tile (once) and of K and V^T blocks into three-stage rings;
-//   warp 5:    the MMA issuer: S(n) = Q K(n)^T into TMEM buffer n % 2 (kind::f8f6f4, K = 32 per
-//              instruction), then O += P(n-1) V(n-1) (A = P from shared memory, B = the V^T
-//              block, both K-major), so S of the next block overlaps the softmax of this one.
-// Scales: S = (Q8 K8^T) q_scale[row] k_scale[block] enters the softmax as one multiplier per row
-// and block; v_scale (per sequence and kv head) multiplies O at the end, together with 1 / l.
+// GB300 mapping: one CTA per pair of 128-row packed Q tiles (tokens x the g query heads of a
+// kv head), 320 threads:
+//   warps 0-7: the softmax, warps 4t..4t+3 for tile t, one thread per row (TMEM lane quarter =
+//              warp % 4).  S of a key block is pulled into registers whole, so its TMEM region
+//              is free again at once; P goes to shared memory as e4m3 bytes of 16 P~ (P~ <= 2^4
+//              with the lazy rescale below, so 16 P~ <= 256 stays inside e4m3's range and its
+//              normal grid covers P~ >= 2^-10);
+//   warp 8:    TMA of the two Q tiles (once) and of K and V^T blocks into three-stage rings,
+//              each block serving both tiles;
+//   warp 9:    the MMA issuer: S_t(n) = Q_t K(n)^T (kind::f8f6f4, K = 32 per instruction) as
+//              soon as tile t's softmax holds S_t(n-1) in registers, then O_t += P_t(n-1) V(n-1)
+//              (A = P from shared memory, B = the V^T block, both K-major).
+//   TMEM: tile t has S at [256 t, 256 t + 128) and O at [256 t + 128, 256 t + 256).
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -29,7 +30,7 @@ namespace attn {
 
 namespace {
 
-constexpr int kF8Threads = 192;
+constexpr int kF8Threads = 320;
 constexpr int kF8Stages = 3;
 constexpr int kAtom = 128 * 128;      // 128 rows x 128 bytes, 128-byte swizzle
 constexpr float kPLog2 = 4.f;         // P is stored as 2^4 P~
@@ -39,20 +40,21 @@ struct F8Bars {
     uint64_t q_full;
     uint64_t k_full[kF8Stages], k_empty[kF8Stages];
     uint64_t v_full[kF8Stages], v_empty[kF8Stages];
-    uint64_t s_full[2], s_free[2];
-    uint64_t p_full[2], p_empty[2];
-    uint64_t pv_done, o_done, drain;
+    uint64_t s_full[2], s_free[2];          // per tile
+    uint64_t p_full[2][2], p_empty[2][2];   // per tile and P buffer
+    uint64_t pv_done[2];                    // per tile
+    uint64_t o_done, drain;
     uint32_t tmem_base;
     int kb0;
     int abort_flag;
 };
 
-// Shared memory: Q tile, K ring, V^T ring, two P buffers (each one atom), barriers.
+// Shared memory: two Q tiles, K ring, V^T ring, two P buffers per tile (one atom each), barriers.
 constexpr int kOffQ = 0;
-constexpr int kOffK = kAtom;
+constexpr int kOffK = 2 * kAtom;
 constexpr int kOffV = kOffK + kF8Stages * kAtom;
 constexpr int kOffP = kOffV + kF8Stages * kAtom;
-constexpr int kOffBars = kOffP + 2 * kAtom;
+constexpr int kOffBars = kOffP + 4 * kAtom;
 constexpr int kF8Smem = kOffBars + static_cast<int>(sizeof(F8Bars)) + 1024;
 static_assert(kF8Smem <= 227 * 1024, "FP8 forward shared memory");
 
@@ -77,11 +79,29 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
         if (threadIdx.x == 0) atomicOr(p.status, kStatusBounds);
         return;
     }
-    const int i = gridDim.x - 1 - blockIdx.x;  // the tiles that see the most keys go first
-    if (i * p.tpt >= Lq) return;
-    const int imin = i * p.tpt, imax = min(imin + p.tpt, Lq) - 1;
-    const KvRange kr_ = kv_block_range(imin, imax, Lq, Lk, 128, p.causal, p.wl, p.wr);
-    const int lo = kr_.lo, hi = kr_.hi;
+    // the pairs of tiles that see the most keys go first
+    const int tile0 = 2 * (gridDim.x - 1 - blockIdx.x);
+    if (tile0 * p.tpt >= Lq) return;
+    // key blocks seen by either tile (consecutive tiles see overlapping or adjacent ranges)
+    int lo, hi;
+    {
+        const KvRange r0 = kv_block_range(tile0 * p.tpt, min(tile0 * p.tpt + p.tpt, Lq) - 1, Lq,
+                                          Lk, 128, p.causal, p.wl, p.wr);
+        lo = r0.lo;
+        hi = r0.hi;
+        if ((tile0 + 1) * p.tpt < Lq) {
+            const KvRange r1 = kv_block_range((tile0 + 1) * p.tpt,
+                                              min((tile0 + 2) * p.tpt, Lq) - 1, Lq, Lk, 128,
+                                              p.causal, p.wl, p.wr);
+            if (hi <= lo) {
+                lo = r1.lo;
+                hi = r1.hi;
+            } else if (r1.hi > r1.lo) {
+                lo = min(lo, r1.lo);
+                hi = max(hi, r1.hi);
+            }
+        }
+    }
 
     if (threadIdx.x == 0) {
         // first 128-key block of this sequence in the V^T columns and the k_scale rows
@@ -95,13 +115,15 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
             mbar_init(&bars->v_full[s], 1);
             mbar_init(&bars->v_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars->s_full[s], 1);
-            mbar_init(&bars->s_free[s], 4);
-            mbar_init(&bars->p_full[s], 4);
-            mbar_init(&bars->p_empty[s], 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&bars->s_full[t], 1);
+            mbar_init(&bars->s_free[t], 4);
+            mbar_init(&bars->pv_done[t], 1);
+            for (int s = 0; s < 2; ++s) {
+                mbar_init(&bars->p_full[t][s], 4);
+                mbar_init(&bars->p_empty[t][s], 1);
+            }
         }
-        mbar_init(&bars->pv_done, 1);
         mbar_init(&bars->o_done, 1);
         mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
@@ -113,20 +135,21 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
         if (threadIdx.x == 0) atomicOr(p.status, kStatusBounds);
         return;
     }
-    if (warp == 5) tmem_alloc(&bars->tmem_base, 512);
+    if (warp == 9) tmem_alloc(&bars->tmem_base, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     const Watchdog wd{&bars->abort_flag, p.status};
-    constexpr uint32_t kColO = 256;  // S buffers at columns 0 and 128
 
-    if (warp == 4) {
+    if (warp == 8) {
         if (lane == 0 && hi > lo) {
             tma_prefetch_desc(&p.tm_k);
             tma_prefetch_desc(&p.tm_v);
-            mbar_arrive_expect_tx(&bars->q_full, 128u * p.g * p.tpt);
-            tma_load_3d(smem + kOffQ, &p.tm_q, &bars->q_full, 0, kvh * p.g, q0 + imin);
+            mbar_arrive_expect_tx(&bars->q_full, 2 * 128u * p.g * p.tpt);
+            tma_load_3d(smem + kOffQ, &p.tm_q, &bars->q_full, 0, kvh * p.g, q0 + tile0 * p.tpt);
+            tma_load_3d(smem + kOffQ + kAtom, &p.tm_q, &bars->q_full, 0, kvh * p.g,
+                        q0 + (tile0 + 1) * p.tpt);
             int nk = 0, nv = 0;
             for (int j = lo; j < hi; ++j) {
                 const int sk = nk % kF8Stages;
@@ -148,40 +171,49 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
             for (int m = nv > kF8Stages ? nv - kF8Stages : 0; m < nv; ++m)
                 f8_drain(&bars->v_full[m % kF8Stages], (m / kF8Stages) & 1);
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         if (lane == 0) {
             constexpr uint32_t kId = idesc_e4m3_f32(128, 128);
-            const uint64_t qd = sdesc_sw128(smem_u32(smem + kOffQ), 16, 1024);
-            // O += P(m) V(m): K-steps of 32 keys (32 bytes) along both K-major operands
+            // O_t += P_t(m) V(m) for both tiles: K-steps of 32 keys (32 bytes) along both
+            // K-major operands
             auto pv = [&](int m) {
                 const int sv = m % kF8Stages, bm = m & 1;
-                if (!wd.wait(&bars->p_full[bm], (m >> 1) & 1) ||
-                    !wd.wait(&bars->v_full[sv], (m / kF8Stages) & 1))
-                    return false;
-                tc_fence_after();
-                const uint64_t pd = sdesc_sw128(smem_u32(smem + kOffP + bm * kAtom), 16, 1024);
+                if (!wd.wait(&bars->v_full[sv], (m / kF8Stages) & 1)) return false;
                 const uint64_t vd = sdesc_sw128(smem_u32(smem + kOffV + sv * kAtom), 16, 1024);
+                for (int t = 0; t < 2; ++t) {
+                    if (!wd.wait(&bars->p_full[t][bm], (m >> 1) & 1)) return false;
+                    tc_fence_after();
+                    const uint64_t pd =
+                        sdesc_sw128(smem_u32(smem + kOffP + (2 * t + bm) * kAtom), 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    umma_ss_f8(tmem + kColO, pd + 2 * kk, vd + 2 * kk, kId, (m > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&bars->p_empty[bm]);
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_ss_f8(tmem + 256 * t + 128, pd + 2 * kk, vd + 2 * kk, kId,
+                                   (m > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(&bars->p_empty[t][bm]);
+                    umma_commit(&bars->pv_done[t]);
+                }
                 umma_commit(&bars->v_empty[sv]);
-                umma_commit(&bars->pv_done);
                 return true;
             };
             int n = 0;
             bool ok = hi > lo && wd.wait(&bars->q_full, 0);
             for (int j = lo; ok && j < hi; ++j) {
-                const int sk = n % kF8Stages, bn = n & 1;
-                ok = wd.wait(&bars->k_full[sk], (n / kF8Stages) & 1) &&
-                     (n < 2 || wd.wait(&bars->s_free[bn], ((n - 2) >> 1) & 1));
+                const int sk = n % kF8Stages;
+                ok = wd.wait(&bars->k_full[sk], (n / kF8Stages) & 1);
                 if (!ok) break;
-                tc_fence_after();
                 const uint64_t kd = sdesc_sw128(smem_u32(smem + kOffK + sk * kAtom), 16, 1024);
+                for (int t = 0; t < 2 && ok; ++t) {
+                    // S_t(n) over S_t(n-1), which tile t's softmax holds in registers
+                    ok = n == 0 || wd.wait(&bars->s_free[t], (n - 1) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t qd = sdesc_sw128(smem_u32(smem + kOffQ + t * kAtom), 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    umma_ss_f8(tmem + 128 * bn, qd + 2 * kk, kd + 2 * kk, kId, kk > 0 ? 1u : 0u);
-                umma_commit(&bars->s_full[bn]);
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_ss_f8(tmem + 256 * t, qd + 2 * kk, kd + 2 * kk, kId, kk > 0 ? 1u : 0u);
+                    umma_commit(&bars->s_full[t]);
+                }
+                if (!ok) break;
                 umma_commit(&bars->k_empty[sk]);
                 if (n >= 1 && !pv(n - 1)) {
                     ok = false;
@@ -195,11 +227,16 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
             f8_drain(&bars->drain, 0);
         }
     } else {
-        // softmax: thread = packed row r of the tile
-        const int r = threadIdx.x;
-        const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+        // softmax: tile t, thread = packed row r of the tile
+        const int t = warp >> 2, quarter = warp & 3;
+        const int r = 32 * quarter + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
+        const uint32_t col_s = 256 * t, col_o = 256 * t + 128;
+        const int imin = (tile0 + t) * p.tpt;
+        const bool tile_ok = imin < Lq;
+        const int imax = tile_ok ? min(imin + p.tpt, Lq) - 1 : imin;
         const int tok = imin + r / p.g, head = kvh * p.g + r % p.g;
-        const bool valid = r < p.g * p.tpt && tok < Lq;
+        const bool valid = tile_ok && r < p.g * p.tpt && tok < Lq;
         int kmin = 1, kmax = 0;
         float qs = 0.f;
         if (valid) {
@@ -207,8 +244,9 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
             qs = p.q_scale[static_cast<size_t>(head) * p.nqb + (q0 + tok) / 128];
         }
         const float* ks_row = p.k_scale + static_cast<size_t>(kvh) * p.nkb + kb0;
-        // this thread's row of the P buffers: 128 keys as bytes, 16-byte chunk c at c ^ (r % 8)
-        const uint32_t row_p = smem_u32(smem + kOffP) + r * 128;
+        // this thread's row of the tile's P buffers: 128 keys as bytes, 16-byte chunk c at
+        // c ^ (r % 8)
+        const uint32_t row_p = smem_u32(smem + kOffP + 2 * t * kAtom) + r * 128;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         int n = 0;
@@ -218,13 +256,13 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
                                                           p.wl, p.wr);
             // (kept positive so that a masked -inf never meets a zero multiplier)
             const float c = fmaxf(qs * ks_row[j] * p.scale_log2, 1.17549435e-38f);
-            ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->s_full[bn], (n >> 1) & 1));
+            ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->s_full[t], n & 1));
             tc_fence_after();
             uint32_t s[128];
             if (ok) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                    tmem_ld32(tmem + lane_off + 128 * bn + 32 * q,
+                    tmem_ld32(tmem + lane_off + col_s + 32 * q,
                               *reinterpret_cast<uint32_t(*)[32]>(s + 32 * q));
                 tmem_wait_ld();
             } else {
@@ -233,7 +271,7 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->s_free[bn]);
+            if (lane == 0) mbar_arrive(&bars->s_free[t]);
             if (masked) {
 #pragma unroll
                 for (int e = 0; e < 128; ++e) {
@@ -242,10 +280,14 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
                 }
             }
             // row maximum of the raw scores (c > 0 keeps the order)
-            float mx = -INFINITY;
+            // (four independent chains)
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int e = 0; e < 128; e += 2)
-                mx = fmax3(mx, __uint_as_float(s[e]), __uint_as_float(s[e + 1]));
+            for (int e = 0; e < 128; e += 8)
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    mq[u] = fmax3(mq[u], __uint_as_float(s[e + 2 * u]), __uint_as_float(s[e + 2 * u + 1]));
+            const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
             const float xm = mx == -INFINITY ? -INFINITY : mx * c;
             // lazy rescale: move m only when the block's maximum exceeds it by > 2^4
             const bool grow = xm > m_used + kLazyLog2;
@@ -256,53 +298,56 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
                 m_used = xm;
             }
             if (__any_sync(0xffffffffu, grow && alpha != 1.f) && n > 0) {
-                // O holds earlier blocks: wait for the last P V, then scale its rows
-                ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->pv_done, (n - 1) & 1));
+                // O_t holds earlier blocks: wait for its last P V, then scale its rows
+                ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->pv_done[t], (n - 1) & 1));
                 tc_fence_after();
                 if (ok) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t o[32];
-                        tmem_ld32(tmem + lane_off + kColO + 32 * q, o);
+                    // in 8-column pieces: the block's 128 scores stay live meanwhile
+#pragma unroll 1
+                    for (int q = 0; q < 16; ++q) {
+                        uint32_t o[8];
+                        tmem_ld8(tmem + lane_off + col_o + 8 * q, o);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(tmem + lane_off + kColO + 32 * q, o);
+                        for (int e = 0; e < 8; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st8(tmem + lane_off + col_o + 8 * q, o);
                     }
                     tmem_wait_st();
                 }
             }
-            // P = 2^4 exp2(x - m), x = s c; an empty row so far uses m = 0 (no -inf - -inf)
-            const float off = kPLog2 - (m_used == -INFINITY ? 0.f : m_used);
-            const uint64_t c2 = f2_make(c, c), off2 = f2_make(off, off);
-            uint32_t pk[32];
-            float sum = 0.f;
-#pragma unroll
-            for (int e = 0; e < 128; e += 4) {
-                float x0, x1, x2, x3;
-                f2_split(f2_fma(f2_make(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), c2, off2), x0, x1);
-                f2_split(f2_fma(f2_make(__uint_as_float(s[e + 2]), __uint_as_float(s[e + 3])), c2, off2), x2, x3);
-                x0 = ex2_approx(x0);
-                x1 = ex2_approx(x1);
-                x2 = ex2_approx(x2);
-                x3 = ex2_approx(x3);
-                sum += (x0 + x1) + (x2 + x3);
-                pk[e / 4] = pack_e4m3x4(x0, x1, x2, x3);
-            }
-            l += sum;
             // buffer bn is free once P V of block n - 2 has read it
             if (n >= 2)
-                ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->p_empty[bn], ((n - 2) >> 1) & 1));
-            if (ok) {
-                const uint32_t row = row_p + bn * kAtom;
+                ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->p_empty[t][bn], ((n - 2) >> 1) & 1));
+            // P = 2^4 exp2(x - m), x = s c; an empty row so far uses m = 0 (no -inf - -inf);
+            // each 16 keys go to shared memory as they are done
+            const float off = kPLog2 - (m_used == -INFINITY ? 0.f : m_used);
+            const uint64_t c2 = f2_make(c, c), off2 = f2_make(off, off);
+            const uint32_t row = row_p + bn * kAtom;
+            float su[4] = {0.f, 0.f, 0.f, 0.f};  // four independent partial sums
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc)
-                    st_shared_v4(row + static_cast<uint32_t>(((cc ^ (r & 7)) * 16)), pk[4 * cc],
-                                 pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-                fence_proxy_async_smem();
+            for (int cc = 0; cc < 8; ++cc) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int e = 16 * cc + 4 * u;
+                    float x0, x1, x2, x3;
+                    f2_split(f2_fma(f2_make(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), c2, off2), x0, x1);
+                    f2_split(f2_fma(f2_make(__uint_as_float(s[e + 2]), __uint_as_float(s[e + 3])), c2, off2), x2, x3);
+                    x0 = ex2_approx(x0);
+                    x1 = ex2_approx(x1);
+                    x2 = ex2_approx(x2);
+                    x3 = ex2_approx(x3);
+                    su[u] += (x0 + x1) + (x2 + x3);
+                    pk[u] = pack_e4m3x4(x0, x1, x2, x3);
+                }
+                if (ok)
+                    st_shared_v4(row + static_cast<uint32_t>(((cc ^ (r & 7)) * 16)), pk[0], pk[1],
+                                 pk[2], pk[3]);
             }
+            l += (su[0] + su[1]) + (su[2] + su[3]);
+            if (ok) fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->p_full[bn]);
+            if (lane == 0) mbar_arrive(&bars->p_full[t][bn]);
         }
         // Epilogue: O = v_scale O~ / l as bf16, LSE = ln 2 (m + log2 l - 4).
         if (n > 0) {
@@ -316,7 +361,7 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
         for (int q = 0; q < 4; ++q) {
             uint32_t o[32];
             if (n > 0 && ok) {
-                tmem_ld32(tmem + lane_off + kColO + 32 * q, o);
+                tmem_ld32(tmem + lane_off + col_o + 32 * q, o);
                 tmem_wait_ld();
             } else {
 #pragma unroll
@@ -340,7 +385,7 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -349,7 +394,8 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
 }  // namespace
 
 cudaError_t launch_fwd_fp8(const Fp8Params& p, cudaStream_t stream) {
-    const dim3 grid((p.max_seqlen_q + p.tpt - 1) / p.tpt, p.batch * p.Hkv);
+    const int tiles = (p.max_seqlen_q + p.tpt - 1) / p.tpt;
+    const dim3 grid((tiles + 1) / 2, p.batch * p.Hkv);
     cudaFuncSetAttribute(fwd_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kF8Smem);
     if (grid.x > 0 && grid.y > 0) fwd_fp8_kernel<<<grid, kF8Threads, kF8Smem, stream>>>(p);
     return cudaGetLastError();
