@@ -450,6 +450,32 @@ def run_ours(args, rank, world, local):
         extra["bwd"] = {"workload": "backward of " + synth.CONFIG_NAMES[2], "ms": round(ms, 4),
                         "tflops": round(fl / ms / 1e9, 2)}
         del bq, bk, bv, bo, bdo, gq, gk, gv
+        # the causal prefill workload's shape with FP8 e4m3 inputs and block scales
+        c = synth.fp8_bench_case()
+        f8 = [x.to(dev) for x in (c.q8, c.k8, c.v8t, c.q_scale, c.k_scale, c.v_scale,
+                                  c.cu_seqlens_q, c.cu_seqlens_k)]
+        fo = torch.empty((c.q8.shape[0], c.q8.shape[1], c.q8.shape[2]), dtype=torch.bfloat16,
+                         device=dev)
+        fl_ = torch.empty((c.q8.shape[1], c.q8.shape[0]), dtype=torch.float32, device=dev)
+
+        def run_f():
+            binding.attn_fwd_fp8(*f8, c.max_seqlen_q, c.max_seqlen_k, c.softmax_scale, c.causal,
+                                 out=fo, lse=fl_)
+        for _ in range(5):
+            run_f()
+        reps = 20
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            run_f()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        ql = (c.cu_seqlens_q[1:] - c.cu_seqlens_q[:-1]).tolist()
+        fl = workload.prefill_flops(ql, ql, c.q8.shape[1], c.q8.shape[2], c.causal)
+        extra["fp8"] = {"workload": synth.FP8_NAME, "ms": round(ms, 4),
+                        "tflops": round(fl / ms / 1e9, 2)}
+        del f8, fo, fl_
     return dict(p_flops=p_flops, d_bytes=d_bytes, total_ms=total_ms, pre_ms=pre_ms,
                 dec_ms=dec_ms, e2e_pre=e2e_pre, e2e_dec=e2e_dec, h2d_pre=h2d_pre,
                 d2h_pre=d2h_pre, h2d_dec=h2d_dec, d2h_dec=d2h_dec, clocks=clk, splits=splits,
