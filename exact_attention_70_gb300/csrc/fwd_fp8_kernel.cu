@@ -250,12 +250,15 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         int n = 0;
+        float ks_next = hi > lo ? ks_row[lo] : 0.f;  // each block's K scale, loaded a block ahead
         for (int j = lo; j < hi; ++j, ++n) {
             const int bn = n & 1;
+            const float ks = ks_next;
+            if (j + 1 < hi) ks_next = ks_row[j + 1];
             const bool masked = !valid || kv_block_masked(j, imin, imax, Lq, Lk, 128, p.causal,
                                                           p.wl, p.wr);
             // (kept positive so that a masked -inf never meets a zero multiplier)
-            const float c = fmaxf(qs * ks_row[j] * p.scale_log2, 1.17549435e-38f);
+            const float c = fmaxf(qs * ks * p.scale_log2, 1.17549435e-38f);
             ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->s_full[t], n & 1));
             tc_fence_after();
             uint32_t s[128];
