@@ -715,3 +715,58 @@ int oracle_f64_to_e4m3(double x) {
     }
     return sign | best;
 }
+
+/* ---- FP8 quantization with block scales and the optional rotation ------------------------ */
+
+/*
+ * "Attention kernels: FlashAttention and PagedAttention", section 四.2 (FlashAttention-3): the
+ * FP8 inputs carry one scale per block, and "incoherent processing" multiplies Q and K by the
+ * same random orthogonal matrix (Q K^T is unchanged) to spread outliers before they are
+ * rounded.  The orthogonal matrix taken here is the normalised Walsh-Hadamard matrix times a
+ * diagonal of random signs, the usual construction of that kind; the signs are an input.
+ *
+ * Walsh-Hadamard transform of n = 2^k values in place (Sylvester order), fp32: stages
+ * h = 1, 2, ..., n/2; in each, every pair (i, i + h) with i & h == 0 becomes
+ * (x_i + x_{i+h}, x_i - x_{i+h}).
+ */
+static void fwht_f32(float* x, int n) {
+    for (int h = 1; h < n; h <<= 1)
+        for (int i = 0; i < n; ++i)
+            if ((i & h) == 0) {
+                const float a = x[i], b = x[i + h];
+                x[i] = a + b;
+                x[i + h] = a - b;
+            }
+}
+
+/*
+ * One block of n rows of d bf16 values (row-major bits) to e4m3 codes and one fp32 scale:
+ *   1. optionally each row x -> H (signs * x) / sqrt(d) (fp32, 1/sqrt(d) rounded to fp32 once);
+ *   2. amax = max |x| over the block; scale = amax / 448 in fp32 (1 for an all-zero block);
+ *   3. code = the e4m3 code nearest to x / scale (fp32 quotient), ties to even, saturating.
+ * Every fp32 operation is a single IEEE operation, so a device implementation doing the same
+ * operations gets the same bits.
+ */
+int oracle_fp8_quantize_rows(const uint16_t* src, long long n, int d, const float* signs,
+                             uint8_t* codes, float* scale) {
+    if (n < 0 || d <= 0 || (d & (d - 1)) != 0) return -1;
+    float* buf = (float*)malloc(sizeof(float) * (size_t)(n > 0 ? n : 1) * (size_t)d);
+    if (!buf) return -1;
+    const float inv = (float)(1.0 / sqrt((double)d));
+    float amax = 0.f;
+    for (long long r = 0; r < n; ++r) {
+        float* x = buf + r * d;
+        for (int e = 0; e < d; ++e) x[e] = (float)bf16_to_f64(src[r * d + e]);
+        if (signs) {
+            for (int e = 0; e < d; ++e) x[e] = x[e] * signs[e];
+            fwht_f32(x, d);
+            for (int e = 0; e < d; ++e) x[e] = x[e] * inv;
+        }
+        for (int e = 0; e < d; ++e) amax = fabsf(x[e]) > amax ? fabsf(x[e]) : amax;
+    }
+    const float s = amax > 0.f ? amax / 448.f : 1.f;
+    for (long long i = 0; i < n * d; ++i) codes[i] = (uint8_t)oracle_f64_to_e4m3((double)(buf[i] / s));
+    *scale = s;
+    free(buf);
+    return 0;
+}

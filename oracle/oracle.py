@@ -87,6 +87,8 @@ def _load():
             lib.oracle_e4m3_to_f64.argtypes = [i32]
             lib.oracle_f64_to_e4m3.restype = i32
             lib.oracle_f64_to_e4m3.argtypes = [dbl]
+            lib.oracle_fp8_quantize_rows.restype = i32
+            lib.oracle_fp8_quantize_rows.argtypes = [P, ll, i32, P, P, P]
             lib.oracle_kvcache_prefill.restype = i32
             lib.oracle_kvcache_prefill.argtypes = [P, P, P, i32, P, P, P, P, i32, i32, i32, P,
                                                    i32, i32, i32, i32, P, P, i32, i32, i32, dbl,
@@ -450,3 +452,63 @@ def fp8_attn_fwd(q8, k8, v8t, q_scale, k_scale, v_scale, cu_seqlens_q, cu_seqlen
                         window_left, window_right)
     return attn_fwd_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, softmax_scale, rows[0], rows[1],
                          causal, window_left, window_right)
+
+
+def fp8_quantize_rows(rows_bf16_bits, signs=None):
+    """One block: rows [n, d] of bf16 bits (uint16) -> (codes uint8 [n, d], scale float)."""
+    a = np.ascontiguousarray(rows_bf16_bits, dtype=np.uint16)
+    n, d = a.shape
+    codes = np.zeros((n, d), np.uint8)
+    sc = np.zeros((1,), np.float32)
+    sg = None if signs is None else np.ascontiguousarray(signs, dtype=np.float32)
+    rc = _load().oracle_fp8_quantize_rows(_ptr(a), n, d, None if sg is None else _ptr(sg),
+                                          _ptr(codes), _ptr(sc))
+    if rc != 0:
+        raise ValueError("oracle_fp8_quantize_rows rejected its arguments")
+    return codes, float(sc[0])
+
+
+def fp8_quantize(q, k, v, cu_seqlens_k, signs=None, key_blocks=None):
+    """bf16 Q, K, V -> the FP8 inputs of fp8_attn_fwd, block by block:
+    q8, q_scale (128 packed tokens per block and head; Q rotated when signs is given),
+    k8, k_scale (128 keys of a sequence per block and kv head; K rotated likewise),
+    v8t, v_scale (V transposed into whole 128-key blocks per sequence, one scale per
+    (sequence, kv head); columns past a sequence's keys are code 0)."""
+    import torch
+    qa, _ = _host(q)
+    ka, _ = _host(k)
+    va, _ = _host(v)
+    total_q, Hq, d = qa.shape
+    total_k, Hkv, _ = ka.shape
+    cu = _i32(cu_seqlens_k).astype(np.int64)
+    batch = len(cu) - 1
+    kb0 = key_block_offsets(cu)
+    nkb = int(kb0[-1]) if key_blocks is None else int(key_blocks)
+    nqb = (total_q + 127) // 128
+    q8 = np.zeros((total_q, Hq, d), np.uint8)
+    qs = np.zeros((Hq, nqb), np.float32)
+    for h in range(Hq):
+        for blk in range(nqb):
+            t0, t1 = 128 * blk, min(total_q, 128 * blk + 128)
+            c, s_ = fp8_quantize_rows(qa[t0:t1, h, :], signs)
+            q8[t0:t1, h, :] = c
+            qs[h, blk] = s_
+    k8 = np.zeros((total_k, Hkv, d), np.uint8)
+    ks = np.ones((Hkv, max(nkb, 1)), np.float32)
+    v8t = np.zeros((Hkv, d, 128 * max(nkb, 1)), np.uint8)
+    vs = np.ones((batch, Hkv), np.float32)
+    for b in range(batch):
+        k0, k1 = int(cu[b]), int(cu[b + 1])
+        for h in range(Hkv):
+            for i in range((k1 - k0 + 127) // 128):
+                t0, t1 = k0 + 128 * i, min(k1, k0 + 128 * i + 128)
+                c, s_ = fp8_quantize_rows(ka[t0:t1, h, :], signs)
+                k8[t0:t1, h, :] = c
+                ks[h, kb0[b] + i] = s_
+            if k1 > k0:
+                c, s_ = fp8_quantize_rows(va[k0:k1, h, :])
+                col = 128 * kb0[b]
+                v8t[h, :, col:col + (k1 - k0)] = c.T
+                vs[b, h] = s_
+    t = torch.from_numpy
+    return t(q8), t(qs), t(k8), t(ks), t(v8t), t(vs)

@@ -131,3 +131,104 @@ def test_fp8_scales_act_linearly():
     out3, lse3 = oracle.fp8_attn_fwd(cq, ck, cv, qs, ks, vs, cu_q, cu_k, 0.10, causal=True)
     np.testing.assert_allclose(out2, out3, rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(lse2, lse3, rtol=1e-12, atol=1e-12)
+
+
+# ---- the quantizer (block scales and the optional random-sign Hadamard rotation) ----------
+
+def _bf16_bits(x):
+    return torch.tensor(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_rotation_is_the_sylvester_hadamard_matrix():
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    d = 128
+    H = scipy_linalg.hadamard(d)
+    for j in (0, 1, 5, 64, 127):
+        x = np.zeros((1, d), np.float32)
+        x[0, j] = 1.0
+        codes, s = oracle.fp8_quantize_rows(_bf16_bits(x), signs=np.ones(d, np.float32))
+        # H e_j / sqrt(d) = column j of H over sqrt(d): every entry has magnitude amax -> 448
+        assert s == np.float32(np.float32(1.0 / math.sqrt(d)) / np.float32(448.0))
+        expect = np.where(H[:, j] > 0, 0x7E, 0xFE)
+        assert np.array_equal(codes[0], expect)
+    # the signs multiply before the transform: signs = e_j-indicator flips column j
+    sg = np.ones(d, np.float32)
+    sg[3] = -1.0
+    x = np.zeros((1, d), np.float32)
+    x[0, 3] = 1.0
+    codes, _ = oracle.fp8_quantize_rows(_bf16_bits(x), signs=sg)
+    assert np.array_equal(codes[0], np.where(H[:, 3] > 0, 0xFE, 0x7E))
+
+
+def test_block_quantization_grid_and_extremes():
+    g = np.random.default_rng(4)
+    x = g.standard_normal((100, 128)).astype(np.float32) * 3.0
+    bits = _bf16_bits(x)
+    xb = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+    codes, s = oracle.fp8_quantize_rows(bits)
+    assert s == np.float32(np.float32(np.abs(xb).max()) / np.float32(448.0))
+    i = np.unravel_index(np.abs(xb).argmax(), xb.shape)
+    assert codes[i] in (0x7E, 0xFE)                       # the block's largest element
+    dec = oracle.e4m3_to_f64(codes)
+    y = (xb / s).astype(np.float64)
+    pos = oracle.e4m3_to_f64(np.arange(0x7F))
+    step = np.array([pos[min(np.searchsorted(pos, abs(v)), 0x7E)] - pos[max(np.searchsorted(pos, abs(v)) - 1, 0)]
+                     for v in y.ravel()]).reshape(y.shape)
+    assert np.all(np.abs(dec - y) <= step / 2 + 1e-12)  # nearest grid point
+    zc, zs = oracle.fp8_quantize_rows(np.zeros((3, 128), np.uint16))
+    assert zs == 1.0 and not zc.any()
+
+
+def test_rotation_preserves_norms_and_attention():
+    c = _rotation_case()
+    g = np.random.default_rng(11)
+    signs = np.where(g.integers(0, 2, 128) > 0, 1.0, -1.0).astype(np.float32)
+    # row norms survive the orthogonal rotation (up to the e4m3 rounding)
+    q8, qs, k8, ks, v8t, vs = oracle.fp8_quantize(c.q, c.k, c.v, c.cu_seqlens_k, signs=signs)
+    q, k, v = oracle.fp8_dequantize(q8, k8, v8t, qs, ks, vs, c.cu_seqlens_k)
+    qf = c.q.double().numpy()
+    np.testing.assert_allclose(np.linalg.norm(q, axis=2), np.linalg.norm(qf, axis=2), rtol=2 ** -4)
+    # and Q K^T: attention on the rotated, quantized inputs tracks the bf16 attention
+    out, lse = oracle.fp8_attn_fwd(q8, k8, v8t, qs, ks, vs, c.cu_seqlens_q, c.cu_seqlens_k,
+                                   c.softmax_scale, causal=True)
+    ref, ref_l = oracle.attn_fwd(c.q, c.k, c.v, c.cu_seqlens_q, c.cu_seqlens_k,
+                                 c.softmax_scale, causal=True)
+    # (V's own e4m3 rounding allows 2^-4 max|V| per element; a rotation that did not cancel
+    # in Q K^T would scramble the scores and move the mean error to order 1)
+    vmax = float(np.abs(c.v.double().numpy()).max())
+    good = np.abs(out - ref).mean()
+    assert np.abs(out - ref).max() <= 2 ** -4 * vmax and good < 0.01
+    # (a single score carries the full Q and K rounding, about 2 * 2^-4 of |q||k| scale)
+    assert np.abs(lse - ref_l).mean() < 0.01 and np.abs(lse - ref_l).max() < 0.2
+    # the control: the same quantizer without the rotation on K (only Q rotated) breaks it
+    q8b, qsb, _, _, _, _ = oracle.fp8_quantize(c.q, c.k, c.v, c.cu_seqlens_k, signs=signs)
+    _, _, k8u, ksu, _, _ = oracle.fp8_quantize(c.q, c.k, c.v, c.cu_seqlens_k)
+    bad, _ = oracle.fp8_attn_fwd(q8b, k8u, v8t, qsb, ksu, vs, c.cu_seqlens_q, c.cu_seqlens_k,
+                                 c.softmax_scale, causal=True)
+    assert np.abs(bad - ref).mean() > 10 * good
+    # with V unrotated and the same rows, quantize -> dequantize returns V to within e4m3 steps
+    vf = c.v.double().numpy()
+    assert np.all(np.abs(v - vf) <= 2 ** -4 * np.abs(vf) + float(vs.max()) * 2 ** -9)
+
+
+def _rotation_case():
+    from exact_attention_70_gb300 import synth
+    return synth.prefill_case([70, 200], 4, 2, 128, True, 21)
+
+
+def test_quantize_layout_round_trip():
+    from exact_attention_70_gb300 import synth
+    c = synth.prefill_case([5, 130, 300], 4, 2, 128, True, 22)
+    q8, qs, k8, ks, v8t, vs = oracle.fp8_quantize(c.q, c.k, c.v, c.cu_seqlens_k)
+    kb0 = oracle.key_block_offsets(c.cu_seqlens_k)
+    assert ks.shape == (2, int(kb0[-1])) and v8t.shape == (2, 128, 128 * int(kb0[-1]))
+    # padding columns of V^T are code 0
+    cu = c.cu_seqlens_k.tolist()
+    for b in range(3):
+        n = cu[b + 1] - cu[b]
+        col = 128 * int(kb0[b])
+        assert not v8t[:, :, col + n:128 * int(kb0[b + 1])].any()
+    q, k, v = oracle.fp8_dequantize(q8, k8, v8t, qs, ks, vs, c.cu_seqlens_k)
+    for got, ref, sc in ((q, c.q, qs), (k, c.k, ks), (v, c.v, vs)):
+        r = ref.double().numpy()
+        assert np.all(np.abs(got - r) <= 2 ** -4 * np.abs(r) + float(sc.max()) * 2 ** -9)
