@@ -63,6 +63,8 @@ def load():
             lib.attn_fwd_kvcache.argtypes = [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, P, P,
                                              i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                              ctypes.c_float, i32, i32, i32, P, sz, P]
+            lib.attn_quantize_fp8.restype = i32
+            lib.attn_quantize_fp8.argtypes = [P] * 4 + [i32] * 8 + [P] * 8
             lib.attn_fwd_fp8.restype = i32
             lib.attn_fwd_fp8.argtypes = [P] * 10 + [i32] * 9 + [f32, i32, i32, i32, P]
             lib.attn_fwd_mods.restype = i32
@@ -224,6 +226,35 @@ def attn_fwd_mods(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_
     if rc != 0:
         raise AttnError(rc, "attn_fwd_mods")
     return out, lse
+
+
+def attn_quantize_fp8(q, k, v, cu_seqlens_k, max_seqlen_k, signs=None, key_blocks=None,
+                      stream=None):
+    """bf16 q, k, v (d = 128) -> (q8, q_scale, k8, k_scale, v8t, v_scale) for attn_fwd_fp8.
+    signs: fp32 [128] CUDA tensor of +-1 (rotate Q and K) or None.  key_blocks defaults to
+    ceil(total_k / 128) + batch."""
+    lib = load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, torch.bfloat16, 3)
+    if signs is not None:
+        _check(signs, "signs", torch.float32, 1)
+    total_q, Hq, d = q.shape
+    total_k, Hkv, _ = k.shape
+    batch = cu_seqlens_k.numel() - 1
+    kb = (total_k + 127) // 128 + batch if key_blocks is None else int(key_blocks)
+    dev = q.device
+    q8 = torch.empty((total_q, Hq, d), dtype=torch.uint8, device=dev)
+    qs = torch.empty((Hq, max(1, (total_q + 127) // 128)), dtype=torch.float32, device=dev)
+    k8 = torch.empty((total_k, Hkv, d), dtype=torch.uint8, device=dev)
+    ks = torch.empty((Hkv, kb), dtype=torch.float32, device=dev)
+    v8t = torch.empty((Hkv, d, 128 * kb), dtype=torch.uint8, device=dev)
+    vs = torch.empty((max(batch, 1), Hkv), dtype=torch.float32, device=dev)
+    rc = lib.attn_quantize_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_k), batch, total_q,
+                               total_k, int(max_seqlen_k), Hq, Hkv, d, kb, _ptr(signs), _ptr(q8),
+                               _ptr(qs), _ptr(k8), _ptr(ks), _ptr(v8t), _ptr(vs), _stream(stream))
+    if rc != 0:
+        raise AttnError(rc, "attn_quantize_fp8")
+    return q8, qs, k8, ks, v8t, vs
 
 
 def attn_fwd_fp8(q8, k8, v8t, q_scale, k_scale, v_scale, cu_seqlens_q, cu_seqlens_k,

@@ -14,7 +14,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libattn.so")
-SOURCES = ["attn_api.cu", "fwd_kernel.cu", "decode_kernel.cu", "decode_noalloc.cu", "selftest.cu", "kvcache.cu", "bwd_kernel.cu", "fwd_fp8_kernel.cu"]
+SOURCES = ["attn_api.cu", "fwd_kernel.cu", "decode_kernel.cu", "decode_noalloc.cu", "selftest.cu", "kvcache.cu", "bwd_kernel.cu", "fwd_fp8_kernel.cu", "quantize_fp8.cu"]
 HEADERS = ["ptx.cuh", "kernels.h", "tile_math.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

@@ -345,6 +345,54 @@ attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
     return ATTN_OK;
 }
 
+attn_status_t attn_quantize_fp8(const void* q, const void* k, const void* v,
+                                const int32_t* cu_seqlens_k, int batch, int total_q, int total_k,
+                                int max_seqlen_k, int nheads_q, int nheads_kv, int head_dim,
+                                int key_blocks, const float* signs, void* q8, float* q_scale,
+                                void* k8, float* k_scale, void* v8t, float* v_scale,
+                                void* stream) {
+    if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_k < 0 || nheads_q <= 0 ||
+        nheads_kv <= 0 || key_blocks < 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+    if (static_cast<long long>(total_q) * nheads_q > (1LL << 31) - 1 ||
+        static_cast<long long>(total_k) * nheads_kv > (1LL << 31) - 1 ||
+        static_cast<long long>(key_blocks) > 65535 || nheads_q > 65535 ||
+        static_cast<long long>(batch) * nheads_kv > 65535 || (total_q + 127) / 128 > (1 << 30))
+        return ATTN_ERR_UNSUPPORTED;
+    if (batch == 0 && total_q == 0) return ATTN_OK;
+    if (!q || !k || !v || !cu_seqlens_k || !q8 || !q_scale || !k8 || !k_scale || !v8t ||
+        !v_scale)
+        return ATTN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(q8, 16) ||
+        !aligned(k8, 16) || !aligned(v8t, 16) || !aligned(q_scale, 4) || !aligned(k_scale, 4) ||
+        !aligned(v_scale, 4) || !aligned(cu_seqlens_k, 4) || (signs && !aligned(signs, 4)))
+        return ATTN_ERR_INVALID_ARG;
+    QuantParams qp;
+    memset(&qp, 0, sizeof(qp));
+    qp.q = static_cast<const __nv_bfloat16*>(q);
+    qp.k = static_cast<const __nv_bfloat16*>(k);
+    qp.v = static_cast<const __nv_bfloat16*>(v);
+    qp.cu_k = cu_seqlens_k;
+    qp.signs = signs;
+    qp.q8 = static_cast<uint8_t*>(q8);
+    qp.k8 = static_cast<uint8_t*>(k8);
+    qp.v8t = static_cast<uint8_t*>(v8t);
+    qp.q_scale = q_scale;
+    qp.k_scale = k_scale;
+    qp.v_scale = v_scale;
+    qp.batch = batch;
+    qp.total_q = total_q;
+    qp.total_k = total_k;
+    qp.max_seqlen_k = max_seqlen_k;
+    qp.Hq = nheads_q;
+    qp.Hkv = nheads_kv;
+    qp.key_blocks = key_blocks;
+    if (launch_quantize_fp8(qp, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
 size_t attn_fwd_kvcache_workspace_bytes(int batch, int total_q, int max_seqlen_q, int nheads_q,
                                         int nheads_kv, int head_dim, int rotary_dim) {
     const size_t list = attn_fwd_workspace_bytes(batch, max_seqlen_q, nheads_q, nheads_kv);

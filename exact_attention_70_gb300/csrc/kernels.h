@@ -141,6 +141,25 @@ struct Fp8Params {
 
 cudaError_t launch_fwd_fp8(const Fp8Params& p, cudaStream_t stream);
 
+// bf16 Q, K, V -> the FP8 forward's inputs (layouts as above); signs: fp32 [128] of +-1 for
+// the rotation of Q and K, or null.
+struct QuantParams {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const int* cu_k;
+    const float* signs;
+    uint8_t* q8;
+    uint8_t* k8;
+    uint8_t* v8t;
+    float* q_scale;
+    float* k_scale;
+    float* v_scale;
+    int batch, total_q, total_k, max_seqlen_k, Hq, Hkv, key_blocks;
+};
+
+cudaError_t launch_quantize_fp8(const QuantParams& p, cudaStream_t stream);
+
 // ---- failure-path self-test ------------------------------------------------------------
 
 cudaError_t launch_watchdog_selftest(unsigned* status, cudaStream_t stream);

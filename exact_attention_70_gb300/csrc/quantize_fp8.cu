@@ -1,0 +1,251 @@
+// quantize_fp8.cu -- bf16 Q, K, V to the FP8 (e4m3) inputs of the FP8 forward pass.
+//
+// The method ("Attention kernels: FlashAttention and PagedAttention", section 四.2,
+// FlashAttention-3): Q, K and V are rounded to e4m3 with one scale per block, after the
+// optional "incoherent processing" that multiplies Q and K by the same random orthogonal matrix
+// (here H diag(signs) / sqrt(d), H the Walsh-Hadamard matrix), and V is re-laid out key-major.
+// For a block: amax = max |x|, scale = amax / 448 (1 when the block is zero), code = e4m3(x /
+// scale), round to nearest even, saturating.  Every fp32 step is one IEEE operation.
+//
+// Layouts (as the FP8 forward reads them):
+//   q8 [total_q, Hq, d], q_scale [Hq, ceil(total_q / 128)]: blocks of 128 packed tokens;
+//   k8 [total_k, Hkv, d], k_scale [Hkv, key_blocks]: blocks of 128 keys of one sequence,
+//       block kb0[b] + i (kb0 the prefix sum of ceil(Lk_b / 128)); unused blocks get scale 1;
+//   v8t [Hkv, d, 128 key_blocks]: V transposed, key t of sequence b in column
+//       128 kb0[b] + (t - k0), zero elsewhere; v_scale [batch, Hkv]: one per sequence and head.
+// Kernels: quant_rows_kernel (Q or K, one CTA per block and head, a warp per 16 rows, four
+// values per lane, the transform's butterflies across lanes by shuffles), quant_v_amax_kernel
+// (atomic max of |V| per sequence and head), quant_v_kernel (one CTA per key block and head,
+// transposed through shared memory), quant_v_finalize_kernel (amax -> scale).  All of it is
+// bandwidth-bound: each input byte is read once (V twice) and each output byte written once.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace attn {
+
+namespace {
+
+constexpr int kQThreads = 256;  // 8 warps x 16 rows = one 128-row block
+constexpr float kInvSqrt128 = 0.0883883476483184405f;  // 1 / sqrt(128), rounded to fp32 once
+
+// Sequence b holding key block blk of the per-sequence numbering, and the block's index i
+// within it; b = batch when blk is past the last sequence's blocks.
+__device__ __forceinline__ void key_block_owner(const int* cu_k, int batch, int blk, int& b,
+                                                int& i) {
+    int kb0 = 0;
+    for (b = 0; b < batch; ++b) {
+        const int nb = (cu_k[b + 1] - cu_k[b] + 127) / 128;
+        if (blk < kb0 + nb) {
+            i = blk - kb0;
+            return;
+        }
+        kb0 += nb;
+    }
+    i = 0;
+}
+
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+    return pack_e4m3x4(a, b, c, d);
+}
+
+// One block of up to 128 rows (token rows t0.., of head h) of a [total, H, 128] bf16 tensor.
+// kKeys: blocks are 128 keys of a sequence (K); otherwise 128 consecutive tokens (Q).
+template <bool kKeys>
+__global__ void __launch_bounds__(kQThreads) quant_rows_kernel(const __nv_bfloat16* __restrict__ src,
+                                                                uint8_t* __restrict__ dst,
+                                                                float* __restrict__ scale,
+                                                                const int* __restrict__ cu_k,
+                                                                const float* __restrict__ signs,
+                                                                int batch, int total, int H,
+                                                                int nblocks) {
+    const int blk = blockIdx.x, h = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int t0 = 128 * blk, t1 = min(total, t0 + 128);
+    if (kKeys) {
+        int b, i;
+        key_block_owner(cu_k, batch, blk, b, i);
+        if (b >= batch) {  // a block past the sequences: scale 1, no codes
+            if (threadIdx.x == 0) scale[static_cast<size_t>(h) * nblocks + blk] = 1.f;
+            return;
+        }
+        t0 = cu_k[b] + 128 * i;
+        t1 = min(min(cu_k[b + 1], t0 + 128), total);  // (rows are clamped to the tensor)
+        if (t0 < 0) t0 = t1;
+    }
+    float sg[4] = {1.f, 1.f, 1.f, 1.f};
+    if (signs != nullptr) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sg[k] = signs[4 * lane + k];
+    }
+    // this warp's 16 rows, four consecutive values per lane
+    float x[16][4];
+    float amax = 0.f;
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr) {
+        const int t = t0 + 16 * warp + rr;
+        if (t < t1) {
+            const uint2 u = *reinterpret_cast<const uint2*>(src + (static_cast<size_t>(t) * H + h) * 128 + 4 * lane);
+            x[rr][0] = __uint_as_float(u.x << 16);
+            x[rr][1] = __uint_as_float(u.x & 0xFFFF0000u);
+            x[rr][2] = __uint_as_float(u.y << 16);
+            x[rr][3] = __uint_as_float(u.y & 0xFFFF0000u);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) x[rr][k] = 0.f;
+        }
+        if (signs != nullptr) {
+            // element i = 4 lane + k; stages h = 1, 2 inside the lane, h = 4 .. 64 across lanes
+#pragma unroll
+            for (int k = 0; k < 4; ++k) x[rr][k] = __fmul_rn(x[rr][k], sg[k]);
+            float a, c;
+            a = x[rr][0]; c = x[rr][1]; x[rr][0] = __fadd_rn(a, c); x[rr][1] = __fsub_rn(a, c);
+            a = x[rr][2]; c = x[rr][3]; x[rr][2] = __fadd_rn(a, c); x[rr][3] = __fsub_rn(a, c);
+            a = x[rr][0]; c = x[rr][2]; x[rr][0] = __fadd_rn(a, c); x[rr][2] = __fsub_rn(a, c);
+            a = x[rr][1]; c = x[rr][3]; x[rr][1] = __fadd_rn(a, c); x[rr][3] = __fsub_rn(a, c);
+#pragma unroll
+            for (int m = 1; m < 32; m <<= 1) {
+                const bool upper = (lane & m) != 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float other = __shfl_xor_sync(0xffffffffu, x[rr][k], m);
+                    // pair (lower, upper) -> (lower + upper, lower - upper)
+                    x[rr][k] = upper ? __fsub_rn(other, x[rr][k]) : __fadd_rn(x[rr][k], other);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) x[rr][k] = __fmul_rn(x[rr][k], kInvSqrt128);
+        }
+        if (t < t1) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fabsf(x[rr][k]));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    __shared__ float red[kQThreads / 32];
+    if (lane == 0) red[warp] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int w = 1; w < kQThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+    const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    if (threadIdx.x == 0) scale[static_cast<size_t>(h) * nblocks + blk] = s;
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr) {
+        const int t = t0 + 16 * warp + rr;
+        if (t < t1)
+            *reinterpret_cast<uint32_t*>(dst + (static_cast<size_t>(t) * H + h) * 128 + 4 * lane) =
+                e4m3x4(__fdiv_rn(x[rr][0], s), __fdiv_rn(x[rr][1], s), __fdiv_rn(x[rr][2], s),
+                       __fdiv_rn(x[rr][3], s));
+    }
+}
+
+// max |V| per (sequence, kv head), as fp32 bits, into amax[b * Hkv + h] (zeroed first).
+__global__ void __launch_bounds__(256) quant_v_amax_kernel(const __nv_bfloat16* __restrict__ v,
+                                                           const int* __restrict__ cu_k,
+                                                           unsigned* __restrict__ amax_bits,
+                                                           int Hkv, int total_k) {
+    const int b = blockIdx.y / Hkv, h = blockIdx.y % Hkv;
+    const int k0 = max(cu_k[b], 0), k1 = min(cu_k[b + 1], total_k);
+    const int t0 = k0 + 128 * blockIdx.x;
+    float m = 0.f;
+    for (int idx = threadIdx.x; idx < 128 * 32; idx += blockDim.x) {  // 128 rows x 32 lanes of 4
+        const int t = t0 + idx / 32;
+        if (t >= k1) break;
+        const uint2 u = *reinterpret_cast<const uint2*>(v + (static_cast<size_t>(t) * Hkv + h) * 128 + 4 * (idx % 32));
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(__uint_as_float(u.x << 16)), fabsf(__uint_as_float(u.x & 0xFFFF0000u))),
+                           fmaxf(fabsf(__uint_as_float(u.y << 16)), fabsf(__uint_as_float(u.y & 0xFFFF0000u)))));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((threadIdx.x & 31) == 0 && m > 0.f) atomicMax(amax_bits + blockIdx.y, __float_as_uint(m));
+}
+
+// One 128-key block of V for kv head h: codes with the sequence's scale, written transposed
+// (v8t row = one of the d dimensions, 128 key columns); padding keys and unused blocks are 0.
+__global__ void __launch_bounds__(256) quant_v_kernel(const __nv_bfloat16* __restrict__ v,
+                                                      const int* __restrict__ cu_k,
+                                                      const unsigned* __restrict__ amax_bits,
+                                                      uint8_t* __restrict__ v8t, int batch,
+                                                      int Hkv, int key_blocks, int total_k) {
+    __shared__ uint32_t tile[128][33];  // [d][key / 4] codes, padded against bank conflicts
+    const int blk = blockIdx.x, h = blockIdx.y;
+    int b, i;
+    key_block_owner(cu_k, batch, blk, b, i);
+    int t0 = 0, n = 0;
+    float s = 1.f;
+    if (b < batch) {
+        t0 = max(cu_k[b], 0) + 128 * i;
+        n = max(0, min(min(cu_k[b + 1], total_k) - t0, 128));  // (rows are clamped to the tensor)
+        const float amax = __uint_as_float(amax_bits[static_cast<size_t>(b) * Hkv + h]);
+        s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    }
+    // thread: key group kg (4 consecutive keys) and d-quad dq; codes of 4 keys x 4 dims
+    for (int w = threadIdx.x; w < 32 * 32; w += blockDim.x) {
+        const int kg = w / 32, dq = w % 32;
+        float x[4][4];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const int key = 4 * kg + kk;
+            if (key < n) {
+                const uint2 u = *reinterpret_cast<const uint2*>(v + (static_cast<size_t>(t0 + key) * Hkv + h) * 128 + 4 * dq);
+                x[kk][0] = __uint_as_float(u.x << 16);
+                x[kk][1] = __uint_as_float(u.x & 0xFFFF0000u);
+                x[kk][2] = __uint_as_float(u.y << 16);
+                x[kk][3] = __uint_as_float(u.y & 0xFFFF0000u);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) x[kk][e] = 0.f;
+            }
+        }
+        // for dimension 4 dq + e: bytes of keys 4 kg .. 4 kg + 3
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            tile[4 * dq + e][kg] = e4m3x4(__fdiv_rn(x[0][e], s), __fdiv_rn(x[1][e], s),
+                                          __fdiv_rn(x[2][e], s), __fdiv_rn(x[3][e], s));
+    }
+    __syncthreads();
+    const size_t cols = static_cast<size_t>(128) * key_blocks;
+    for (int w = threadIdx.x; w < 128 * 32; w += blockDim.x) {
+        const int dd = w / 32, kg = w % 32;
+        *reinterpret_cast<uint32_t*>(v8t + (static_cast<size_t>(h) * 128 + dd) * cols + 128 * static_cast<size_t>(blk) + 4 * kg) =
+            tile[dd][kg];
+    }
+}
+
+__global__ void quant_v_finalize_kernel(float* v_scale, int n) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) {
+        const float amax = v_scale[i];  // holds the amax bits
+        v_scale[i] = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_fp8(const QuantParams& p, cudaStream_t stream) {
+    const int nqb = (p.total_q + 127) / 128;
+    if (nqb > 0)
+        quant_rows_kernel<false><<<dim3(nqb, p.Hq), kQThreads, 0, stream>>>(
+            p.q, p.q8, p.q_scale, p.cu_k, p.signs, p.batch, p.total_q, p.Hq, nqb);
+    if (p.key_blocks > 0)
+        quant_rows_kernel<true><<<dim3(p.key_blocks, p.Hkv), kQThreads, 0, stream>>>(
+            p.k, p.k8, p.k_scale, p.cu_k, p.signs, p.batch, p.total_k, p.Hkv, p.key_blocks);
+    cudaError_t e = cudaMemsetAsync(p.v_scale, 0, sizeof(float) * p.batch * p.Hkv, stream);
+    if (e != cudaSuccess) return e;
+    const int vb = (p.max_seqlen_k + 127) / 128;
+    if (vb > 0 && p.batch > 0)
+        quant_v_amax_kernel<<<dim3(vb, p.batch * p.Hkv), 256, 0, stream>>>(
+            p.v, p.cu_k, reinterpret_cast<unsigned*>(p.v_scale), p.Hkv, p.total_k);
+    if (p.key_blocks > 0)
+        quant_v_kernel<<<dim3(p.key_blocks, p.Hkv), 256, 0, stream>>>(
+            p.v, p.cu_k, reinterpret_cast<const unsigned*>(p.v_scale), p.v8t, p.batch, p.Hkv,
+            p.key_blocks, p.total_k);
+    const int n = p.batch * p.Hkv;
+    if (n > 0) quant_v_finalize_kernel<<<(n + 255) / 256, 256, 0, stream>>>(p.v_scale, n);
+    return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -267,6 +267,26 @@ attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
                            int head_dim, int key_blocks, float softmax_scale, int causal,
                            int window_left, int window_right, void* stream);
 
+/*
+ * bf16 Q, K, V to the inputs of attn_fwd_fp8 (same page and section): for each block,
+ * amax = max |x|, scale = amax / 448 (1 for an all-zero block), code = e4m3(x / scale), round to
+ * nearest even and saturating, each step one IEEE fp32 operation.
+ *   q, k, v      device bf16 [total_q, nheads_q, 128], [total_k, nheads_kv, 128] x 2
+ *   signs        device fp32 [128] of +1 / -1, or NULL: Q and K rows are first rotated by
+ *                H diag(signs) / sqrt(128) (H the Walsh-Hadamard matrix, "incoherent
+ *                processing"; Q K^T is unchanged); V is never rotated
+ *   key_blocks   >= sum_b ceil(Lk_b / 128), e.g. ceil(total_k / 128) + batch
+ *   outputs      q8, q_scale, k8, k_scale, v8t, v_scale in the layouts attn_fwd_fp8 reads;
+ *                unused key blocks get scale 1 and zero V^T columns
+ * cu_seqlens_k as attn_fwd (rows outside [0, total_k) are never read); head_dim must be 128.
+ */
+attn_status_t attn_quantize_fp8(const void* q, const void* k, const void* v,
+                                const int32_t* cu_seqlens_k, int batch, int total_q, int total_k,
+                                int max_seqlen_k, int nheads_q, int nheads_kv, int head_dim,
+                                int key_blocks, const float* signs, void* q8, float* q_scale,
+                                void* k8, float* k_scale, void* v8t, float* v_scale,
+                                void* stream);
+
 /* Bytes of split-partial workspace for attn_decode_kvcache; num_splits 0 sizes for the
  * automatic choice (at most 16 splits).  0 when one split needs no workspace. */
 size_t attn_decode_workspace_bytes(int batch, int nheads_q, int head_dim, int num_splits);

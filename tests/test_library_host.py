@@ -248,3 +248,23 @@ def test_fp8_arguments_are_checked(lib):
     assert call(3, P(4098)) == -1           # misaligned q_scale
     assert call(21, -2) == -1               # window
     assert call(10, 0) == 0                 # batch 0
+
+
+def test_quantize_arguments_are_checked(lib):
+    P = ctypes.c_void_p
+    fake = P(4096)
+    f = lib.attn_quantize_fp8
+    # q k v cu_k | batch total_q total_k max_k Hq Hkv d key_blocks | signs q8 qs k8 ks v8t vs stream
+    base = [fake] * 4 + [1, 16, 16, 16, 4, 2, 128, 2] + [None, fake, fake, fake, fake, fake, fake, None]
+
+    def call(i, v):
+        a = list(base)
+        a[i] = v
+        return f(*a)
+
+    assert call(10, 64) == -2               # head_dim 64 is not built for FP8
+    assert call(11, -1) == -1               # key_blocks
+    assert call(8, 0) == -1                 # Hq
+    assert call(13, None) == -1             # null q8
+    assert call(12, P(4098)) == -1          # misaligned signs
+    assert call(14, P(4097)) == -1          # misaligned q_scale
