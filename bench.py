@@ -473,9 +473,29 @@ def run_ours(args, rank, world, local):
         ms = a.elapsed_time(b) / reps
         ql = (c.cu_seqlens_q[1:] - c.cu_seqlens_q[:-1]).tolist()
         fl = workload.prefill_flops(ql, ql, c.q8.shape[1], c.q8.shape[2], c.causal)
+        # and the quantizer that produces such inputs from bf16 (rotation of Q and K on)
+        cq_ = synth.config_case(2)
+        bq_, bk_, bv_ = cq_.q.to(dev), cq_.k.to(dev), cq_.v.to(dev)
+        bck_ = cq_.cu_seqlens_k.to(dev)
+        sg_ = torch.where(torch.arange(128, device=dev) % 3 == 0, -1.0, 1.0).float()
+
+        def run_qz():
+            binding.attn_quantize_fp8(bq_, bk_, bv_, bck_, cq_.max_seqlen_k, signs=sg_)
+        for _ in range(3):
+            run_qz()
+        a.record(stream)
+        for _ in range(reps):
+            run_qz()
+        b.record(stream)
+        torch.cuda.synchronize()
+        qms = a.elapsed_time(b) / reps
+        # bytes: Q, K, V read as bf16 (V twice: its maximum, then its codes), codes written
+        qbytes = (bq_.numel() + bk_.numel() + 2 * bv_.numel()) * 2 + bq_.numel() + bk_.numel() + bv_.numel()
         extra["fp8"] = {"workload": synth.FP8_NAME, "ms": round(ms, 4),
-                        "tflops": round(fl / ms / 1e9, 2)}
-        del f8, fo, fl_
+                        "tflops": round(fl / ms / 1e9, 2),
+                        "quantize_ms": round(qms, 4),
+                        "quantize_gbs": round(qbytes / qms / 1e6, 1)}
+        del f8, fo, fl_, bq_, bk_, bv_
     return dict(p_flops=p_flops, d_bytes=d_bytes, total_ms=total_ms, pre_ms=pre_ms,
                 dec_ms=dec_ms, e2e_pre=e2e_pre, e2e_dec=e2e_dec, h2d_pre=h2d_pre,
                 d2h_pre=d2h_pre, h2d_dec=h2d_dec, d2h_dec=d2h_dec, clocks=clk, splits=splits,
