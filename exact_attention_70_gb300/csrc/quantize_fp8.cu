@@ -4,8 +4,9 @@
 // FlashAttention-3): Q, K and V are rounded to e4m3 with one scale per block, after the
 // optional "incoherent processing" that multiplies Q and K by the same random orthogonal matrix
 // (here H diag(signs) / sqrt(d), H the Walsh-Hadamard matrix), and V is re-laid out key-major.
-// For a block: amax = max |x|, scale = amax / 448 (1 when the block is zero), code = e4m3(x /
-// scale), round to nearest even, saturating.  Every fp32 step is one IEEE operation.
+// For a block: amax = max |x|, scale = amax / 448 (1 when the block is zero), code = e4m3(x r)
+// with r = 448 / amax formed once per block, round to nearest even, saturating.  Every fp32
+// step is one IEEE operation.
 //
 // Layouts (as the FP8 forward reads them):
 //   q8 [total_q, Hq, d], q_scale [Hq, ceil(total_q / 128)]: blocks of 128 packed tokens;
@@ -131,14 +132,15 @@ __global__ void __launch_bounds__(kQThreads) quant_rows_kernel(const __nv_bfloat
 #pragma unroll
     for (int w = 1; w < kQThreads / 32; ++w) amax = fmaxf(amax, red[w]);
     const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    const float rcp = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
     if (threadIdx.x == 0) scale[static_cast<size_t>(h) * nblocks + blk] = s;
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) {
         const int t = t0 + 16 * warp + rr;
         if (t < t1)
             *reinterpret_cast<uint32_t*>(dst + (static_cast<size_t>(t) * H + h) * 128 + 4 * lane) =
-                e4m3x4(__fdiv_rn(x[rr][0], s), __fdiv_rn(x[rr][1], s), __fdiv_rn(x[rr][2], s),
-                       __fdiv_rn(x[rr][3], s));
+                e4m3x4(__fmul_rn(x[rr][0], rcp), __fmul_rn(x[rr][1], rcp),
+                       __fmul_rn(x[rr][2], rcp), __fmul_rn(x[rr][3], rcp));
     }
 }
 
@@ -175,12 +177,12 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const __nv_bfloat16* __res
     int b, i;
     key_block_owner(cu_k, batch, blk, b, i);
     int t0 = 0, n = 0;
-    float s = 1.f;
+    float rcp = 1.f;
     if (b < batch) {
         t0 = max(cu_k[b], 0) + 128 * i;
         n = max(0, min(min(cu_k[b + 1], total_k) - t0, 128));  // (rows are clamped to the tensor)
         const float amax = __uint_as_float(amax_bits[static_cast<size_t>(b) * Hkv + h]);
-        s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+        rcp = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
     }
     // thread: key group kg (4 consecutive keys) and d-quad dq; codes of 4 keys x 4 dims
     for (int w = threadIdx.x; w < 32 * 32; w += blockDim.x) {
@@ -203,8 +205,8 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const __nv_bfloat16* __res
         // for dimension 4 dq + e: bytes of keys 4 kg .. 4 kg + 3
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-            tile[4 * dq + e][kg] = e4m3x4(__fdiv_rn(x[0][e], s), __fdiv_rn(x[1][e], s),
-                                          __fdiv_rn(x[2][e], s), __fdiv_rn(x[3][e], s));
+            tile[4 * dq + e][kg] = e4m3x4(__fmul_rn(x[0][e], rcp), __fmul_rn(x[1][e], rcp),
+                                          __fmul_rn(x[2][e], rcp), __fmul_rn(x[3][e], rcp));
     }
     __syncthreads();
     const size_t cols = static_cast<size_t>(128) * key_blocks;

@@ -269,8 +269,8 @@ attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
 
 /*
  * bf16 Q, K, V to the inputs of attn_fwd_fp8 (same page and section): for each block,
- * amax = max |x|, scale = amax / 448 (1 for an all-zero block), code = e4m3(x / scale), round to
- * nearest even and saturating, each step one IEEE fp32 operation.
+ * amax = max |x|, scale = amax / 448 (1 for an all-zero block), code = e4m3(x * (448 / amax)),
+ * round to nearest even and saturating, each step one IEEE fp32 operation.
  *   q, k, v      device bf16 [total_q, nheads_q, 128], [total_k, nheads_kv, 128] x 2
  *   signs        device fp32 [128] of +1 / -1, or NULL: Q and K rows are first rotated by
  *                H diag(signs) / sqrt(128) (H the Walsh-Hadamard matrix, "incoherent

@@ -743,7 +743,8 @@ static void fwht_f32(float* x, int n) {
  * One block of n rows of d bf16 values (row-major bits) to e4m3 codes and one fp32 scale:
  *   1. optionally each row x -> H (signs * x) / sqrt(d) (fp32, 1/sqrt(d) rounded to fp32 once);
  *   2. amax = max |x| over the block; scale = amax / 448 in fp32 (1 for an all-zero block);
- *   3. code = the e4m3 code nearest to x / scale (fp32 quotient), ties to even, saturating.
+ *   3. code = the e4m3 code nearest to x * r with r = 448 / amax (fp32, formed once per block;
+ *      1 for an all-zero block), ties to even, saturating.
  * Every fp32 operation is a single IEEE operation, so a device implementation doing the same
  * operations gets the same bits.
  */
@@ -765,7 +766,8 @@ int oracle_fp8_quantize_rows(const uint16_t* src, long long n, int d, const floa
         for (int e = 0; e < d; ++e) amax = fabsf(x[e]) > amax ? fabsf(x[e]) : amax;
     }
     const float s = amax > 0.f ? amax / 448.f : 1.f;
-    for (long long i = 0; i < n * d; ++i) codes[i] = (uint8_t)oracle_f64_to_e4m3((double)(buf[i] / s));
+    const float rcp = amax > 0.f ? 448.f / amax : 1.f;
+    for (long long i = 0; i < n * d; ++i) codes[i] = (uint8_t)oracle_f64_to_e4m3((double)(buf[i] * rcp));
     *scale = s;
     free(buf);
     return 0;

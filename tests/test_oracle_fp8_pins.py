@@ -170,7 +170,8 @@ def test_block_quantization_grid_and_extremes():
     i = np.unravel_index(np.abs(xb).argmax(), xb.shape)
     assert codes[i] in (0x7E, 0xFE)                       # the block's largest element
     dec = oracle.e4m3_to_f64(codes)
-    y = (xb / s).astype(np.float64)
+    rcp = np.float32(448.0) / np.float32(np.abs(xb).max())
+    y = np.clip((xb * rcp).astype(np.float64), -448.0, 448.0)  # (beyond 448 saturates)
     pos = oracle.e4m3_to_f64(np.arange(0x7F))
     step = np.array([pos[min(np.searchsorted(pos, abs(v)), 0x7E)] - pos[max(np.searchsorted(pos, abs(v)) - 1, 0)]
                      for v in y.ravel()]).reshape(y.shape)
