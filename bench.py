@@ -67,8 +67,12 @@ def load_peaks():
 
 
 def source_sha(name):
-    with open(os.path.join(ROOT, "exact_attention_70_gb300", "csrc", name), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of a kernel's source file and the headers every kernel inlines."""
+    h = hashlib.sha256()
+    for f in (name, "ptx.cuh", "kernels.h", "tile_math.h"):
+        with open(os.path.join(ROOT, "exact_attention_70_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel, source):
