@@ -47,7 +47,7 @@ struct BwdCfg {
 
 struct BwdBars {
     uint64_t fixed_full;                               // loaded once (dK/dV: K, V; dQ: Q, dO)
-    uint64_t in_full[kKStages], in_empty[kKStages];    // streamed operands (dQ: K)
+    uint64_t in_full[kKStages], in_empty[kKStages];    // streamed operands (dK/dV: Q, dO; dQ: K)
     uint64_t v_full[kStages], v_empty[kStages];        // dQ: V
     uint64_t info_full[kStages], info_empty[kStages];  // row information (dK/dV)
     uint64_t s_full, s_free;                           // dQ: S / dP in TMEM, loaded to registers
