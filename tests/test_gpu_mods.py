@@ -52,3 +52,34 @@ def test_modifiers_match_oracle(attn, idx):
                                         softcap=cap,
                                         alibi_slopes=slopes.double().numpy() if alibi else None)
     compare(out.cpu(), lse.cpu().T, o_ref, l_ref.T, c.name)
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3])
+def test_modifiers_repeatable_with_fresh_buffers(attn, idx):
+    """The same call, repeated with every input re-uploaded to new device buffers and other
+    allocations in between, gives bitwise the same O and LSE, each time within the parity
+    tolerances: catches results that depend on timing or on what memory held before."""
+    lq, lk, Hq, Hkv, d, causal, window, cap, alibi = CASES[idx]
+    c = synth.prefill_case(lq, Hq, Hkv, d, causal, seed=800 + idx, lengths_k=lk, window=window,
+                           name=f"mods{idx}")
+    slopes = torch.tensor([2.0 ** (-8.0 * (h + 1) / Hq) for h in range(Hq)], dtype=torch.float32)
+    o_ref, l_ref = oracle.attn_fwd_mods(c.q, c.k, c.v, c.cu_seqlens_q, c.cu_seqlens_k,
+                                        c.softmax_scale, c.causal, c.window_left, c.window_right,
+                                        softcap=cap, alibi_slopes=slopes.double().numpy())
+    dev = "cuda"
+    first = None
+    for rep in range(12):
+        filler = torch.randn(1 << (14 + rep % 4), device=dev)  # moves the allocator around
+        args = [x.to(dev) for x in (c.q, c.k, c.v, c.cu_seqlens_q, c.cu_seqlens_k)]
+        out, lse = attn.attn_fwd_mods(*args, c.max_seqlen_q, c.max_seqlen_k, c.softmax_scale,
+                                      c.causal, c.window_left, c.window_right, softcap=cap,
+                                      alibi_slopes=slopes.to(dev))
+        torch.cuda.synchronize()
+        assert attn.attn_get_device_status() == 0
+        o, l = out.cpu(), lse.cpu()
+        compare(o, l.T, o_ref, l_ref.T, f"{c.name} rep {rep}")
+        if first is None:
+            first = (o, l)
+        else:
+            assert torch.equal(o, first[0]) and torch.equal(l, first[1]), f"rep {rep} differs"
+        del filler
