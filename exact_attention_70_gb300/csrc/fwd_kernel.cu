@@ -513,11 +513,14 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
                         }
                     }
                 }
-                // row maxima: this thread's 32 values of each row, then across the quad
-                float xa0 = __uint_as_float(s[0]), xa1 = __uint_as_float(s[1]);
-                float xb0 = __uint_as_float(s[2]), xb1 = __uint_as_float(s[3]);
+                // row maxima: this thread's 32 values of each row (16 chunks of 4: chunks 0 and 1
+                // start four chains, then chunks c and c + 1 for even c >= 2 join them), then across the quad
+                float xa0 = fmaxf(__uint_as_float(s[0]), __uint_as_float(s[4]));
+                float xa1 = fmaxf(__uint_as_float(s[1]), __uint_as_float(s[5]));
+                float xb0 = fmaxf(__uint_as_float(s[2]), __uint_as_float(s[6]));
+                float xb1 = fmaxf(__uint_as_float(s[3]), __uint_as_float(s[7]));
 #pragma unroll
-                for (int c = 1; c < 16; c += 2) {
+                for (int c = 2; c < 16; c += 2) {
                     xa0 = fmax3(xa0, __uint_as_float(s[4 * c]), __uint_as_float(s[4 * c + 4]));
                     xa1 = fmax3(xa1, __uint_as_float(s[4 * c + 1]), __uint_as_float(s[4 * c + 5]));
                     xb0 = fmax3(xb0, __uint_as_float(s[4 * c + 2]), __uint_as_float(s[4 * c + 6]));

@@ -104,6 +104,52 @@ def test_prefill_is_deterministic(attn):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+SINGLE_KEY_CASES = [
+    # (lengths, Hq, Hkv, d): causal, so the first token of each sequence sees exactly one key
+    ([300, 77], 4, 2, 128),
+    ([500], 8, 2, 128),
+    ([200, 129], 4, 4, 64),
+    ([1000, 17, 513], 32, 4, 128),
+    ([130, 260], 6, 2, 128),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(SINGLE_KEY_CASES)))
+@pytest.mark.parametrize("mods", [False, True])
+def test_single_visible_key_rows_are_exact(attn, idx, mods):
+    """A row that sees one key has P = (1) whatever the running maximum, so O is that key's V
+    row bit for bit and LSE is its logit: pins the row maximum and the normalisation (a wrong
+    reference maximum shows up here as bf16 rounding of P away from 1)."""
+    lengths, Hq, Hkv, d = SINGLE_KEY_CASES[idx]
+    c = synth.prefill_case(lengths, Hq, Hkv, d, True, seed=1500 + idx, name=f"single{idx}")
+    dev = to_dev(c)
+    cap = 20.0 if mods else 0.0
+    slopes = torch.tensor([2.0 ** (-8.0 * (h + 1) / Hq) for h in range(Hq)], dtype=torch.float32)
+    if mods:
+        out, lse = attn.attn_fwd_mods(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"],
+                                      dev["cu_seqlens_k"], c.max_seqlen_q, c.max_seqlen_k,
+                                      c.softmax_scale, True, -1, -1, softcap=cap,
+                                      alibi_slopes=slopes.cuda())
+    else:
+        out, lse = attn.attn_fwd(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"],
+                                 dev["cu_seqlens_k"], c.max_seqlen_q, c.max_seqlen_k,
+                                 c.softmax_scale, True)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == 0
+    out, lse = out.float().cpu(), lse.cpu().double()
+    g = Hq // Hkv
+    cu = c.cu_seqlens_q.tolist()
+    for b in range(len(cu) - 1):
+        t = cu[b]
+        for h in range(Hq):
+            v_row = c.v[t, h // g].float()
+            assert torch.equal(out[t, h], v_row), f"seq {b} head {h}: O is not V of its one key"
+            x = float((c.q[t, h].double() * c.k[t, h // g].double()).sum()) * c.softmax_scale
+            if mods:
+                x = cap * math.tanh(x / cap)  # the ALiBi bias of the key at distance 0 is 0
+            assert abs(float(lse[h, t]) - x) < 1e-5, f"seq {b} head {h}: LSE {float(lse[h, t])} vs {x}"
+
+
 def test_bounded_wait_reports_timeout_and_context_survives(attn):
     # a wait on a barrier that nothing completes runs out (20 ms limit) and is reported
     assert attn.attn_selftest_wait_timeout() == 0
