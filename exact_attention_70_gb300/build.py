@@ -21,7 +21,7 @@ NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 
 
 def _flags(extra=()):
-    return [NVCC, *ARCH, "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
+    return [NVCC, *ARCH, "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
             f"-I{os.path.join(ROOT, 'include')}", *extra]
 
 
