@@ -753,12 +753,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->s_free);
-            uint32_t pd[32];
-            if (!masked) {
+            uint32_t pd[32];  // computed and stored only when the scores above were loaded
+            if (ok && !masked) {
 #pragma unroll
                 for (int e = 0; e < 64; e += 2)
                     pd[e / 2] = ds_pair(sv[e], sv[e + 1], dv[e], dv[e + 1], scale2, nl2, ndd2);
-            } else {
+            } else if (ok) {
                 const int k0 = j * 128 + 64 * ch;
 #pragma unroll
                 for (int e = 0; e < 64; e += 2) {
