@@ -372,13 +372,9 @@ def attn_fwd_kvcache(q, k_new, v_new, k_cache, v_cache, cache_seqlens, block_tab
     return out, lse
 
 
-def attn_decode_kvcache(q, k_cache, v_cache, cache_seqlens, block_table, softmax_scale=None,
-                        num_splits=0, out=None, lse=None, workspace=None, stream=None):
-    """Decode over a paged cache.  q [batch, Hq, d]; caches [num_pages, page_size, Hkv, d].
-
-    Returns (out [batch, Hq, d] bf16, lse [batch, Hq] fp32).
-    """
-    lib = load()
+def _decode_shapes(q, k_cache, v_cache, cache_seqlens, block_table):
+    """Checks shared by both decode entry points: dtypes, ranks, and one table row and one
+    length per sequence (a short table or length vector would be read past its end)."""
     _check(q, "q", torch.bfloat16, 3)
     _check(k_cache, "k_cache", torch.bfloat16, 4)
     _check(v_cache, "v_cache", torch.bfloat16, 4)
@@ -390,13 +386,33 @@ def attn_decode_kvcache(q, k_cache, v_cache, cache_seqlens, block_table, softmax
         raise ValueError("k_cache and v_cache must both be [num_pages, page_size, Hkv, d]")
     if cache_seqlens.numel() != batch or block_table.shape[0] != batch:
         raise ValueError("cache_seqlens and block_table must have one row per sequence")
-    scale = d ** -0.5 if softmax_scale is None else float(softmax_scale)
+    return batch, Hq, Hkv, d, num_pages, page_size
+
+
+def _decode_outputs(q, out, lse):
+    batch, Hq, _ = q.shape
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((batch, Hq), dtype=torch.float32, device=q.device)
     _check(out, "out", torch.bfloat16, 3)
     _check(lse, "lse", torch.float32, 2)
+    if tuple(out.shape) != tuple(q.shape) or tuple(lse.shape) != (batch, Hq):
+        raise ValueError("out must be [batch, Hq, d] and lse [batch, Hq]")
+    return out, lse
+
+
+def attn_decode_kvcache(q, k_cache, v_cache, cache_seqlens, block_table, softmax_scale=None,
+                        num_splits=0, out=None, lse=None, workspace=None, stream=None):
+    """Decode over a paged cache.  q [batch, Hq, d]; caches [num_pages, page_size, Hkv, d].
+
+    Returns (out [batch, Hq, d] bf16, lse [batch, Hq] fp32).
+    """
+    lib = load()
+    batch, Hq, Hkv, d, num_pages, page_size = _decode_shapes(q, k_cache, v_cache, cache_seqlens,
+                                                             block_table)
+    scale = d ** -0.5 if softmax_scale is None else float(softmax_scale)
+    out, lse = _decode_outputs(q, out, lse)
     nbytes = int(lib.attn_decode_workspace_bytes(batch, Hq, d, int(num_splits)))
     ws = _workspace(nbytes, q.device, workspace)
     rc = lib.attn_decode_kvcache(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_seqlens),
@@ -424,22 +440,10 @@ def attn_decode_kvcache_noalloc(q, k_cache, v_cache, cache_seqlens, block_table,
         P, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         fn.restype = i32
         fn.argtypes = [P, P, P, P, P, i32, i32, P, P, i32, i32, i32, i32, i32, i32, f32, P]
-    _check(q, "q", torch.bfloat16, 3)
-    _check(k_cache, "k_cache", torch.bfloat16, 4)
-    _check(v_cache, "v_cache", torch.bfloat16, 4)
-    _check(cache_seqlens, "cache_seqlens", torch.int32, 1)
-    _check(block_table, "block_table", torch.int32, 2)
-    batch, Hq, d = q.shape
-    num_pages, page_size, Hkv, dk = k_cache.shape
-    if v_cache.shape != k_cache.shape or dk != d:
-        raise ValueError("k_cache and v_cache must both be [num_pages, page_size, Hkv, d]")
+    batch, Hq, Hkv, d, num_pages, page_size = _decode_shapes(q, k_cache, v_cache, cache_seqlens,
+                                                             block_table)
     scale = d ** -0.5 if softmax_scale is None else float(softmax_scale)
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None:
-        lse = torch.empty((batch, Hq), dtype=torch.float32, device=q.device)
-    _check(out, "out", torch.bfloat16, 3)
-    _check(lse, "lse", torch.float32, 2)
+    out, lse = _decode_outputs(q, out, lse)
     rc = fn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_seqlens), _ptr(block_table),
             page_size, int(num_splits), _ptr(out), _ptr(lse), batch, Hq, Hkv, d,
             block_table.shape[1], num_pages, scale, _stream(stream))

@@ -111,11 +111,17 @@ __global__ void __launch_bounds__(kDecThreads, 2)
                 uint8_t* vdst = kdst + C::kKvBytes;
                 for (int pc = 0; pc < pieces; ++pc) {
                     const int tok = c * kDecChunk + pc * p.box_rows;
-                    int page = bt[tok / p.page_size];
-                    if (page < 0 || page >= p.num_pages) {
-                        // an out-of-range id loads zeros (TMA fills outside the tensor)
-                        atomicOr(p.status, kStatusBounds);
-                        page = p.num_pages;
+                    // A piece wholly past the sequence end (possible in the last chunk when
+                    // pages are shorter than a chunk) is aimed past the end of the cache, so
+                    // TMA fills it with zeros and its block_table entry is never read.
+                    int page = p.num_pages;
+                    if (tok < L) {
+                        page = bt[tok / p.page_size];
+                        if (page < 0 || page >= p.num_pages) {
+                            // an out-of-range id loads zeros (TMA fills outside the tensor)
+                            atomicOr(p.status, kStatusBounds);
+                            page = p.num_pages;
+                        }
                     }
                     const int row = page * p.page_size + tok % p.page_size;
 #pragma unroll
@@ -127,13 +133,24 @@ __global__ void __launch_bounds__(kDecThreads, 2)
                     }
                 }
             }
-            // wait for every load still in flight before the ring is reused for the merge
+            // wait for every load still in flight before the ring is reused for the merge; a
+            // load that never lands raises the timeout status and the abort flag, so that
+            // nothing is merged or stored from this CTA
             const uint32_t n_st = issued < C::kStages ? issued : C::kStages;
             for (uint32_t st = 0; st < n_st; ++st) {
                 const uint32_t last = st + C::kStages * ((issued - 1 - st) / C::kStages);
                 const unsigned long long t0 = global_ns();
-                while (!mbar_try(&bars->full[st], (last / C::kStages) & 1))
-                    if (global_ns() - t0 > 200000000ull) break;
+                bool landed = true;
+                while (!mbar_try(&bars->full[st], (last / C::kStages) & 1)) {
+                    if (global_ns() - t0 > kWaitLimitNs) {
+                        landed = false;
+                        break;
+                    }
+                }
+                if (!landed) {
+                    wd.fail();
+                    break;
+                }
             }
         }
     } else {
@@ -256,6 +273,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], 2);
     }
     __syncthreads();  // the ring is idle from here on: reuse it for the cross-warp merge
+    if (wd.aborted()) return;  // a wait ran out: the status word says so, nothing is stored
 
     float* mo = reinterpret_cast<float*>(smem);  // [4 warps][16 rows][kMergeStride]
     float* mm = mo + 4 * kDecRowsPerCta * C::kMergeStride;  // [4][16] running max

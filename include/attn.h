@@ -134,8 +134,10 @@ attn_status_t attn_decode_kvcache(const void* q, const void* k_cache, const void
  * resolved split count, returns ATTN_ERR_WORKSPACE and launches nothing.
  *
  * The first call on a device looks up the array's address on that device (that device must be
- * current); make that first call before any stream capture.  No call allocates or frees device
- * memory.  All calls on a device share the array and it keeps the last call's contents
+ * current); make that first call before any stream capture.  The address is kept for the life
+ * of the process and belongs to the device's primary context, the one the CUDA runtime uses:
+ * do not call this entry point after cudaDeviceReset or with another context of that device
+ * current.  No call allocates or frees device memory.  All calls on a device share the array and it keeps the last call's contents
  * (nothing needs clearing: each call rewrites every slot it reads); calls whose kernels
  * overlap on the GPU race on it, so order them on one stream or by events.
  */
@@ -256,8 +258,11 @@ attn_status_t attn_fwd_mods(const void* q, const void* k, const void* v, void* o
  *   v_scale device fp32 [batch, nheads_kv]: one scale per (sequence, kv head)
  *   key_blocks >= kb0[batch]; a sequence whose blocks run past it sets the device bounds flag.
  * out, lse, cu_seqlens, sizes, causal and window as attn_fwd; head_dim must be 128.  Within
- * the kernel P is rounded to e4m3 (as 16 P~ with P~ <= 16, see the design notes for the bound
- * on O), S and O accumulate in fp32, and LSE is computed from the unrounded P~.
+ * the kernel P is rounded to e4m3 (as 16 P~ with P~ <= 16), S and O accumulate in fp32, and
+ * LSE is computed from the unrounded P~.  The rounding of P is the only approximation added to
+ * the exact attention of the dequantized inputs: each element of O differs from it by at most
+ * 2^-4 sum_j P_j |v_j| (keys in e4m3's normal range, 16 P~ >= 2^-6) plus a term below
+ * 2^-14 |v_j| / l per remaining key, plus the bf16 rounding of O.
  */
 attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
                            const float* q_scale, const float* k_scale, const float* v_scale,

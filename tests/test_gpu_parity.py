@@ -250,3 +250,47 @@ def test_config4_paged_decode(attn):
     o_ref, l_ref = oracle.decode(case.q, case.k_cache, case.v_cache, case.cache_seqlens,
                                  case.block_table, case.softmax_scale, 0, rb, rh)
     compare(out[rb, rh], lse[rb, rh], o_ref, l_ref, "cfg4")
+
+
+PADDED_TABLES = [
+    # (lengths, Hq, Hkv, d, page_size, max_pages): every table entry past a sequence's
+    # ceil(L / page_size) pages is -1, and the table sits at the end of a buffer whose next
+    # entries are -1 too, so any read past a sequence's own pages raises BOUNDS
+    ([20, 40, 33, 47], 8, 2, 128, 16, 3),   # 3 pages x 16 = 48 keys: not a multiple of 64
+    ([1, 17, 100, 250], 8, 2, 128, 32, 9),  # 9 x 32 = 288 keys
+    ([5, 64, 129, 30], 32, 8, 64, 16, 13),  # 13 x 16 = 208 keys, d = 64
+    ([200, 3], 4, 4, 128, 64, 5),
+]
+
+
+def _padded_table_case(idx):
+    lens, Hq, Hkv, d, ps, mp = PADDED_TABLES[idx]
+    case = synth.decode_case(lens, Hq, Hkv, d, ps, seed=310 + idx, max_pages=mp,
+                             name=f"padded{idx}")
+    for b, L in enumerate(lens):
+        case.block_table[b, (L + ps - 1) // ps:] = -1
+    return case
+
+
+def _table_at_buffer_end(bt):
+    buf = torch.full((bt.numel() + 64,), -1, dtype=torch.int32, device="cuda")
+    view = buf[:bt.numel()].view(bt.shape)
+    view.copy_(bt)
+    return view
+
+
+@pytest.mark.parametrize("idx", range(len(PADDED_TABLES)))
+@pytest.mark.parametrize("splits", [0, 1, 3])
+@pytest.mark.parametrize("entry", ["regular", "noalloc"])
+def test_decode_reads_only_the_sequences_own_pages(attn, idx, splits, entry):
+    case = _padded_table_case(idx)
+    d = to_dev(case)
+    bt = _table_at_buffer_end(d["block_table"])
+    fn = attn.attn_decode_kvcache if entry == "regular" else attn.attn_decode_kvcache_noalloc
+    out, lse = fn(d["q"], d["k_cache"], d["v_cache"], d["cache_seqlens"], bt,
+                  case.softmax_scale, splits)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == 0
+    o_ref, l_ref = oracle.decode(case.q, case.k_cache, case.v_cache, case.cache_seqlens,
+                                 case.block_table, case.softmax_scale)
+    compare(out.cpu(), lse.cpu(), o_ref, l_ref, case.name)
