@@ -219,6 +219,7 @@ attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* out, f
     FwdParams fp;
     memset(&fp, 0, sizeof(fp));
     if (encode_3d(&fp.tm_q, q, head_dim, nheads_q, total_q, g, tpt) != ATTN_OK ||
+        encode_3d(&fp.tm_o, out, head_dim, nheads_q, total_q, g, tpt) != ATTN_OK ||
         encode_3d(&fp.tm_k, k, head_dim, nheads_kv, total_k > 0 ? total_k : 1, 1,
                   kFwdBlockN) != ATTN_OK ||
         encode_3d(&fp.tm_v, v, head_dim, nheads_kv, total_k > 0 ? total_k : 1, 1,
@@ -515,6 +516,7 @@ attn_status_t attn_fwd_kvcache(const void* q, const void* k_new, const void* v_n
     memset(&fp, 0, sizeof(fp));
     if (encode_3d(&fp.tm_q, q_rot ? static_cast<const void*>(q_rot) : q, head_dim, nheads_q,
                   total_q, g, tpt) != ATTN_OK ||
+        encode_3d(&fp.tm_o, out, head_dim, nheads_q, total_q, g, tpt) != ATTN_OK ||
         encode_3d(&fp.tm_k, k_cache, head_dim, nheads_kv, cache_rows, 1, box_rows) != ATTN_OK ||
         encode_3d(&fp.tm_v, v_cache, head_dim, nheads_kv, cache_rows, 1, box_rows) != ATTN_OK)
         return ATTN_ERR_CUDA;

@@ -65,13 +65,25 @@ struct FwdCfg {
 
 struct FwdBars {
     uint64_t q_full, q_empty;
-    uint64_t kv_full[8], kv_empty[8];
+    // One ring of K/V slots.  A slot alternates between K and V blocks, and K is consumed by the
+    // S issuer while V is consumed by the PV issuer, so each slot has one "full" barrier per
+    // kind: every waiter then sees every phase of its barrier in order, which is what a parity
+    // wait needs (on a shared barrier the S issuer could wait for a K while the slot's previous
+    // V was still landing, and its parity wait would read the phase before as complete).
+    uint64_t k_full[8], v_full[8], kv_empty[8];
     uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_free[2];
+    uint64_t epi_full[2], epi_free[2];  // O staged in P_t for a TMA store / the store read it
     uint64_t drain[2];
     uint32_t tmem_base;
     int abort_flag;
 };
 static_assert(sizeof(FwdBars) <= 512, "barrier block");
+
+// Per-slot parity of the K (or V) loads a role has seen go into each ring slot: bit s flips at
+// every load of that kind into slot s, and before a wait it is the parity of the awaited phase.
+__device__ __forceinline__ uint32_t slot_parity(uint32_t bits, uint32_t st) {
+    return (bits >> st) & 1u;
+}
 
 // Geometry of one work item, derived identically by every role.
 struct Item {
@@ -156,10 +168,16 @@ __device__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 // ---- TMA producer (one thread) -----------------------------------------------------------
 
+// What the producer has put into the ring: the slot loads so far and, per slot, the parity of
+// its K and of its V loads and whether its latest load was a V.
+struct RingState {
+    uint32_t n = 0, kpar = 0, vpar = 0, lastv = 0;
+};
+
 template <int D, bool kPaged>
 __device__ void fwd_producer_loop(const FwdParams& p, uint8_t* smem, FwdBars* bars,
                                   const Watchdog& wd, int n_items, uint32_t& q_cnt,
-                                  uint32_t& kv_cnt) {
+                                  RingState& ring) {
     using C = FwdCfg<D>;
     tma_prefetch_desc(&p.tm_q);
     tma_prefetch_desc(&p.tm_k);
@@ -192,18 +210,27 @@ __device__ void fwd_producer_loop(const FwdParams& p, uint8_t* smem, FwdBars* ba
             const bool last = r == 2 * m - 1;
             const bool is_v = last || (r > 0 && (r & 1) == 0);
             const int i = is_v ? (last ? m - 1 : (r - 2) / 2) : (r + 1) / 2;
-            const uint32_t n = kv_cnt + r;
+            const uint32_t n = ring.n;
             const uint32_t st = n % C::kSlots;
             if (n >= C::kSlots && !wd.wait(&bars->kv_empty[st], ((n / C::kSlots) - 1) & 1))
                 return;
-            mbar_arrive_expect_tx(&bars->kv_full[st], C::kKvTile);
+            uint64_t* const full = is_v ? &bars->v_full[st] : &bars->k_full[st];
+            mbar_arrive_expect_tx(full, C::kKvTile);
+            ++ring.n;
+            if (is_v) {
+                ring.vpar ^= 1u << st;
+                ring.lastv |= 1u << st;
+            } else {
+                ring.kpar ^= 1u << st;
+                ring.lastv &= ~(1u << st);
+            }
             const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
             uint8_t* const slot = smem + C::kOffKV + st * C::kKvTile;
             if constexpr (!kPaged) {
 #pragma unroll
                 for (int h = 0; h < C::kHalves; ++h)
-                    tma_load_3d(slot + h * C::kAtomBytes, map, &bars->kv_full[st], h * 64,
-                                it.kvh, it.k0 + (it.jlo + i) * kFwdBlockN);
+                    tma_load_3d(slot + h * C::kAtomBytes, map, full, h * 64, it.kvh,
+                                it.k0 + (it.jlo + i) * kFwdBlockN);
             } else {
                 // Gather the block's keys page by page through block_table.  Boxes wholly past
                 // the sequence end (whose table entries need not be valid) and boxes of a bad
@@ -222,12 +249,11 @@ __device__ void fwd_producer_loop(const FwdParams& p, uint8_t* smem, FwdBars* ba
                     }
 #pragma unroll
                     for (int h = 0; h < C::kHalves; ++h)
-                        tma_load_3d(slot + h * C::kAtomBytes + r0 * 128, map, &bars->kv_full[st],
-                                    h * 64, it.kvh, row);
+                        tma_load_3d(slot + h * C::kAtomBytes + r0 * 128, map, full, h * 64,
+                                    it.kvh, row);
                 }
             }
         }
-        kv_cnt += 2 * m;
     }
 }
 
@@ -235,15 +261,20 @@ template <int D, bool kPaged>
 __device__ void fwd_producer(const FwdParams& p, uint8_t* smem, FwdBars* bars,
                              const Watchdog& wd, int n_items) {
     using C = FwdCfg<D>;
-    uint32_t q_cnt = 0, kv_cnt = 0;
-    fwd_producer_loop<D, kPaged>(p, smem, bars, wd, n_items, q_cnt, kv_cnt);
-    // Every slot holds at most one load in flight: wait for the latest load of each one.
+    uint32_t q_cnt = 0;
+    RingState ring;
+    fwd_producer_loop<D, kPaged>(p, smem, bars, wd, n_items, q_cnt, ring);
+    // Every slot holds at most one load in flight: wait for the latest load of each one (its
+    // phase has the parity before that load's flip).
     if (q_cnt > 0) drain_wait(&bars->q_full, (q_cnt - 1) & 1);
-    for (uint32_t st = 0; st < C::kSlots && st < kv_cnt; ++st)
-        drain_wait(&bars->kv_full[st], ((kv_cnt - 1 - st) / C::kSlots) & 1);
+    for (uint32_t st = 0; st < C::kSlots && st < ring.n; ++st) {
+        const bool v = slot_parity(ring.lastv, st) != 0;
+        drain_wait(v ? &bars->v_full[st] : &bars->k_full[st],
+                   slot_parity(v ? ring.vpar : ring.kpar, st) ^ 1u);
+    }
 }
 
-// ---- MMA issuers: warp 9 issues S = Q K^T, warp 10 issues O += P V (one thread each) ------
+// ---- MMA issuers: warp 17 issues S = Q K^T, warp 18 issues O += P V (one thread each) -----
 
 // S_t(j) for every (j, t) of every item.  S_t(j) overwrites the TMEM columns of S_t(j-1), so
 // it waits for tile t's softmax to have read them (s_free).
@@ -259,6 +290,7 @@ __device__ void fwd_mma_s(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint
     const uint32_t kv_lo = static_cast<uint32_t>(dkv);
     const int G = gridDim.x, cta = blockIdx.x;
     uint32_t q_cnt = 0, kv_cnt = 0;
+    uint32_t kpar = 0;                // per-slot parity of the K blocks consumed so far
     uint32_t s_cnt0 = 0, s_cnt1 = 0;  // S_t issued so far
     for (int k = 0; k * G < n_items; ++k) {
         const int idx = item_index(k, cta, G);
@@ -272,7 +304,8 @@ __device__ void fwd_mma_s(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint
             const int j = it.jlo + i;
             const uint32_t n = kv_cnt + ring_pos_k(i);
             const uint32_t st = n % C::kSlots;
-            if (!wd.wait(&bars->kv_full[st], (n / C::kSlots) & 1)) return;
+            if (!wd.wait(&bars->k_full[st], slot_parity(kpar, st))) return;
+            kpar ^= 1u << st;
             const uint32_t k_lo = kv_lo + st * (C::kKvTile >> 4);
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
@@ -312,6 +345,7 @@ __device__ void fwd_mma_pv(const FwdParams& p, uint8_t* smem, FwdBars* bars, uin
     const uint32_t v_lo = static_cast<uint32_t>(dv), v_hi = static_cast<uint32_t>(dv >> 32);
     const int G = gridDim.x, cta = blockIdx.x;
     uint32_t kv_cnt = 0;
+    uint32_t vpar = 0;                    // per-slot parity of the V blocks consumed so far
     uint32_t pv_cnt0 = 0, pv_cnt1 = 0;    // PV_t issued so far (== P_t consumed)
     uint32_t o_items0 = 0, o_items1 = 0;  // items in which tile t accumulated into O_t
     for (int k = 0; k * G < n_items; ++k) {
@@ -325,7 +359,8 @@ __device__ void fwd_mma_pv(const FwdParams& p, uint8_t* smem, FwdBars* bars, uin
             const int j = it.jlo + i;
             const uint32_t n = kv_cnt + ring_pos_v(i, m);
             const uint32_t st = n % C::kSlots;
-            if (!wd.wait(&bars->kv_full[st], (n / C::kSlots) & 1)) return;
+            if (!wd.wait(&bars->v_full[st], slot_parity(vpar, st))) return;
+            vpar ^= 1u << st;
             const uint32_t b_lo = v_lo + st * (C::kKvTile >> 4);
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
@@ -399,6 +434,14 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
     uint64_t* const p_full = &bars->p_full[t];
     uint64_t* const pv_done = &bars->pv_done[t];
     uint64_t* const o_free = &bars->o_free[t];
+    uint64_t* const epi_full = &bars->epi_full[t];
+    uint64_t* const epi_free = &bars->epi_free[t];
+    // Whole tiles leave through a TMA store of the O rows staged in P_t, issued by lane 0 of
+    // the tile's warp 0 and left running; before P_t is written again the tile waits until that
+    // store has read it (epi_free).  epi_cnt counts such stores, epi_pending marks one whose
+    // read has not been waited for yet.
+    uint32_t epi_cnt = 0;
+    bool epi_pending = false;
     const int rbase = 32 * (k & 3) + 16 * (k >> 2);   // this warp's first row
     const int ra = rbase + (lane >> 2);                // this thread's rows ra and ra + 8
     const int cpair = 2 * (lane & 3);                  // its columns in each 8-column chunk
@@ -423,12 +466,19 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
     const int tile_rows = g * p.tpt;
     uint32_t blk = 0;  // blocks of tile t processed so far (== S_t consumed == P_t produced)
     uint32_t kv_cnt = 0;  // K/V ring slots filled for earlier items (locates paged V blocks)
+    uint32_t vpar = 0;    // per-slot parity of the V blocks loaded for earlier items (paged)
     for (int kit = 0; kit * G < n_items; ++kit) {
         const int idx = item_index(kit, cta, G);
         if (idx >= n_items) continue;
         const Item it = load_item<kPaged>(p, idx);
         const uint32_t kv_base = kv_cnt;
-        if (it.any) kv_cnt += 2 * (it.jhi - it.jlo);
+        const uint32_t vpar_item = vpar;
+        if (it.any) {
+            const int m = it.jhi - it.jlo;
+            kv_cnt += 2 * m;
+            if constexpr (kPaged)
+                for (int i = 0; i < m; ++i) vpar ^= 1u << ((kv_base + ring_pos_v(i, m)) % C::kSlots);
+        }
         const TileView tv = tile_view(it, t);
         if (!tv.rows) continue;
         // this thread's rows ra and ra + 8; packed row r is token tok0 + r / g, head kvh g + r % g
@@ -575,9 +625,11 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
                 // warps clear those V rows (whole rows: the swizzle only permutes within a row).
                 if (kPaged && (j + 1) * kFwdBlockN > it.Lk) {
                     const int m = it.jhi - it.jlo;
-                    const uint32_t n = kv_base + ring_pos_v(j - it.jlo, m);
-                    const uint32_t st = n % C::kSlots;
-                    if (!__all_sync(0xffffffffu, wd.wait(&bars->kv_full[st], (n / C::kSlots) & 1)))
+                    uint32_t bits = vpar_item;  // V parities before V_j's load
+                    for (int i = 0; i < j - it.jlo; ++i)
+                        bits ^= 1u << ((kv_base + ring_pos_v(i, m)) % C::kSlots);
+                    const uint32_t st = (kv_base + ring_pos_v(j - it.jlo, m)) % C::kSlots;
+                    if (!__all_sync(0xffffffffu, wd.wait(&bars->v_full[st], slot_parity(bits, st))))
                         return;
                     const int valid = it.Lk - j * kFwdBlockN;
                     const uint32_t vslot = smem_u32(smem + C::kOffKV + st * C::kKvTile);
@@ -612,6 +664,15 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
                     }
                     tmem_wait_st();
                     tc_fence_before();
+                }
+                if (epi_pending) {
+                    // the previous item's O store out of P_t must have read it
+                    if (k == 0 && lane == 0) {
+                        bulk_wait_group_read_all();
+                        mbar_arrive(epi_free);
+                    }
+                    if (!__all_sync(0xffffffffu, wd.wait(epi_free, (epi_cnt - 1) & 1))) return;
+                    epi_pending = false;
                 }
                 // P_t rows of this warp: chunks (2 cp, 2 cp + 1) x (rows ra, ra + 8) per stmatrix
 #pragma unroll
@@ -655,7 +716,25 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_free);
-            if constexpr (!kPaged && !kMods) {
+            if (tv.tok0 + p.tpt <= it.Lq) {
+                // Every packed row of the tile is a row of this sequence: one TMA store per
+                // 64 columns writes the tile's g * tpt rows, asynchronously.
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(epi_full);
+                if (k == 0) {
+                    if (!__all_sync(0xffffffffu, wd.wait(epi_full, epi_cnt & 1))) return;
+                    if (lane == 0) {
+#pragma unroll
+                        for (int h = 0; h < C::kHalves; ++h)
+                            tma_store_3d(&p.tm_o, smem + C::kOffP + t * C::kPTile + h * C::kAtomBytes,
+                                         h * 64, it.kvh * g, it.q0 + tv.tok0);
+                        bulk_commit_group();
+                    }
+                }
+                ++epi_cnt;
+                epi_pending = true;
+            } else if constexpr (!kPaged && !kMods) {
                 // each store instruction writes whole rows: 32 / (D / 8) rows of D / 8 16-byte
                 // units; packed row r is token r / g, head r % g (the quotient taken in fp32:
                 // (r + 1/2) / g is at least 1/(2 g) away from an integer, far beyond the error)
@@ -738,7 +817,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         mbar_init(&bars->q_full, 1);
         mbar_init(&bars->q_empty, 1);
         for (int i = 0; i < C::kSlots; ++i) {
-            mbar_init(&bars->kv_full[i], 1);
+            mbar_init(&bars->k_full[i], 1);
+            mbar_init(&bars->v_full[i], 1);
             mbar_init(&bars->kv_empty[i], 1);
         }
         for (int t = 0; t < 2; ++t) {
@@ -747,6 +827,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             mbar_init(&bars->p_full[t], kSoftmaxWarps / 2);
             mbar_init(&bars->pv_done[t], 1);
             mbar_init(&bars->o_free[t], kSoftmaxWarps / 2);
+            mbar_init(&bars->epi_full[t], kSoftmaxWarps / 2);
+            mbar_init(&bars->epi_free[t], 1);
             mbar_init(&bars->drain[t], 1);
         }
         bars->abort_flag = 0;
@@ -782,6 +864,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     } else {
         regs_increase<104>();
         fwd_softmax<D, kPaged, kMods>(p, smem, bars, tmem, wd, n_items, warp >> 3, warp & 7, lane);
+        // the output stores this thread issued have completed before the CTA's memory goes
+        if ((warp & 7) == 0 && lane == 0) bulk_wait_group_all();
     }
     __syncwarp();
     tc_fence_before();

@@ -46,6 +46,7 @@ struct FwdParams {
     CUtensorMap tm_q;  // 3-D over q   [total_q, Hq, d],  box {64, g, tpt}
     CUtensorMap tm_k;  // 3-D over k   [total_k, Hkv, d], box {64, 1, 128}
     CUtensorMap tm_v;  // 3-D over v   [total_k, Hkv, d], box {64, 1, 128}
+    CUtensorMap tm_o;  // 3-D over out [total_q, Hq, d],  box {64, g, tpt}: stores of whole tiles
     __nv_bfloat16* out;
     float* lse;
     const int* cu_q;
