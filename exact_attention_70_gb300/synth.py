@@ -251,9 +251,12 @@ def chunked_case() -> KvcacheCase:
 # and the 3 mantissa bits uniform, the 4-bit exponent field uniform in [4, 10], i.e. magnitudes
 # log-uniform over [2^-3, 15]; the NaN pattern never occurs.  Scales are uniform in
 # [0.15, 0.25] (decoded values then have an RMS near 1).  V^T columns past a sequence's keys
-# (the layout's padding) are code 0 (value 0).
+# (the layout's padding) are code 0 (value 0).  The full-range variant draws the exponent field
+# uniformly from all 16 values, so zeros, subnormals and +-448 occur (the NaN pattern
+# S.1111.111 is replaced by S.1111.110 = +-448), with scales of 2^-6 that keep the logits in
+# the range a softmax can resolve.
 
-def e4m3_codes(shape, seed: int, stream: int = 0) -> torch.Tensor:
+def e4m3_codes(shape, seed: int, stream: int = 0, full_range: bool = False) -> torch.Tensor:
     """Random e4m3 bit patterns (uint8), reproducible for (shape, seed, stream)."""
     numel = math.prod(shape)
     out = torch.empty(numel, dtype=torch.uint8)
@@ -265,7 +268,11 @@ def e4m3_codes(shape, seed: int, stream: int = 0) -> torch.Tensor:
         bits = torch.randint(0, 1 << 30, (e - s,), generator=g, dtype=torch.int64)
         sign = (bits & 1) << 7
         man = (bits >> 1) & 7
-        exp = 4 + (bits >> 4) % 7
+        if full_range:
+            exp = (bits >> 4) & 15
+            man = torch.where((exp == 15) & (man == 7), torch.full_like(man, 6), man)
+        else:
+            exp = 4 + (bits >> 4) % 7
         out[s:e].copy_((sign | (exp << 3) | man).to(torch.uint8))
 
     if nblk <= 2:
@@ -297,27 +304,28 @@ class Fp8Case:
 
 
 def fp8_case(lengths_q, Hq, Hkv, d, causal, seed, lengths_k=None, window=(-1, -1), scale=None,
-             name="fp8") -> Fp8Case:
+             name="fp8", full_range=False) -> Fp8Case:
     lengths_k = list(lengths_q) if lengths_k is None else list(lengths_k)
     cu_q, cu_k = cu_from_lengths(lengths_q), cu_from_lengths(lengths_k)
     tq, tk = int(cu_q[-1]), int(cu_k[-1])
     blocks = [(int(n) + 127) // 128 for n in lengths_k]
     key_blocks = max(1, sum(blocks))
-    v8t = e4m3_codes((Hkv, d, 128 * key_blocks), seed, 3)
+    v8t = e4m3_codes((Hkv, d, 128 * key_blocks), seed, 3, full_range)
     col = 0
     for n, nb in zip(lengths_k, blocks):   # zero the padding columns of each sequence
         v8t[:, :, col + int(n):col + 128 * nb] = 0
         col += 128 * nb
     v8t[:, :, col:] = 0
     g = torch.Generator().manual_seed(seed * 7 + 5)
+    lo, span = (2.0 ** -6, 2.0 ** -7) if full_range else (0.15, 0.1)
     return Fp8Case(
         name=name,
-        q8=e4m3_codes((tq, Hq, d), seed, 1),
-        k8=e4m3_codes((tk, Hkv, d), seed, 2),
+        q8=e4m3_codes((tq, Hq, d), seed, 1, full_range),
+        k8=e4m3_codes((tk, Hkv, d), seed, 2, full_range),
         v8t=v8t,
-        q_scale=0.15 + 0.1 * torch.rand((Hq, (tq + 127) // 128), generator=g),
-        k_scale=0.15 + 0.1 * torch.rand((Hkv, key_blocks), generator=g),
-        v_scale=0.15 + 0.1 * torch.rand((len(lengths_q), Hkv), generator=g),
+        q_scale=lo + span * torch.rand((Hq, (tq + 127) // 128), generator=g),
+        k_scale=lo + span * torch.rand((Hkv, key_blocks), generator=g),
+        v_scale=lo + span * torch.rand((len(lengths_q), Hkv), generator=g),
         cu_seqlens_q=cu_q, cu_seqlens_k=cu_k,
         max_seqlen_q=max([0] + [int(x) for x in lengths_q]),
         max_seqlen_k=max([0] + [int(x) for x in lengths_k]),

@@ -18,7 +18,7 @@
  *     merged by LSE (section 6.2), causal aligned bottom-right for the kv-cache call
  *     (section 6.2) and the sliding window [i - w_left, i + w_right] (section 7 table).
  *
- * Readings where the pages are silent or disagree (each is also listed in the design notes):
+ * Readings where the pages are silent or disagree:
  *   - causal is aligned bottom-right everywhere: key j is visible to query i iff
  *     j <= i + (Lk - Lq) (+ w_right when not causal); this equals top-left when Lq == Lk;
  *   - window follows the API's (w_left, w_right) pair; -1 means unbounded on that side;

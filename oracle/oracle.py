@@ -377,8 +377,10 @@ def num_threads() -> int:
 # "Attention kernels: FlashAttention and PagedAttention", section 四.2 (FlashAttention-3): Q, K
 # and V go to the 8-bit MMA as e4m3 with block-wise scales, and V is re-laid out so that the
 # PV product reads it key-major.  The oracle decodes the codes (the e4m3 definition above),
-# applies the scales and runs the plain fp64 attention on the values; the e4m3 rounding of P
-# inside the FP8 kernel is an approximation of that result, bounded in the design notes.
+# applies the scales and runs the plain fp64 attention on the values.  The FP8 kernel rounds P
+# to e4m3 before the second product, an approximation of that result whose per-element error is
+# at most 2^-4 sum_j P_j |v_j| (keys in e4m3's normal range) plus a subnormal term and the bf16
+# rounding of O.
 #
 # Scale and layout reading (the page fixes neither):
 #   q_scale [Hq, ceil(total_q / 128)]   one scale per 128 consecutive packed query tokens;

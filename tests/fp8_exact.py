@@ -98,3 +98,66 @@ def check_codes(x, codes, scale, signs=None):
     rel = float(err.max()) / 448.0 + 4 * U32
     assert abs(float(scale) - s_exact) <= rel * s_exact, (float(scale), s_exact)
     return int((near_mid & (got != nearest)).sum())
+
+
+def fp8_forward_bound(q, k, v, cu_q, cu_k, scale, causal, wl, wr, rows=None):
+    """Per-element bound on |O_fp8 - O_ref| for the FP8 forward pass, O_ref being the exact
+    attention of the dequantized fp64 inputs q [tq, Hq, d], k, v [tk, Hkv, d].
+
+    The kernel rounds 16 P~ to e4m3, where P~ = exp2(x - m_ref) and m_ref is a block maximum
+    of the row at most 4 (log2 units) below the true row maximum m, so 1 <= max P~ <= 16 and
+    l~ = sum P~ >= L^ = sum exp2(x - m).  Per key:
+      normal range (16 P~ >= 2^-6): |dP~| <= 2^-4 P~, i.e. 2^-4 P_j after normalisation;
+      subnormal range: |dP~| <= min(P~, 2^-14), i.e. <= min(P^_j, 2^-14) / L^ normalised,
+      which can only happen where P^_j = exp2(x_j - m) < 2^-10.
+    So |dO_i| <= 2^-4 (P|V|)_i + sum_{P^_j < 2^-10} min(P^_j, 2^-14) |v_j| / L^, plus the
+    bf16 rounding of O (2^-9 |O|) and fp32 accumulation (2^-12 (P|V|)_i, generous).
+    Returns (bound, sigma): sigma_i = 2^-4 / sqrt(3) * sqrt(sum_j P_j^2 v_j^2), the standard
+    deviation of the first term when the roundings are independent and uniform.
+    rows = (tok, head) restricts the result to those rows ([n, d]); else [tq, Hq, d]."""
+    q, k, v = (np.asarray(a, np.float64) for a in (q, k, v))
+    tq, Hq, d = q.shape
+    Hkv = k.shape[1]
+    g = Hq // Hkv
+    cu_q = np.asarray(cu_q, np.int64)
+    cu_k = np.asarray(cu_k, np.int64)
+    if rows is None:
+        tt, hh = np.meshgrid(np.arange(tq), np.arange(Hq), indexing="ij")
+        tok, head = tt.ravel(), hh.ravel()
+    else:
+        tok, head = (np.asarray(a, np.int64) for a in rows)
+    bound = np.zeros((len(tok), d))
+    sigma = np.zeros((len(tok), d))
+    seq = np.searchsorted(cu_q, tok, side="right") - 1
+    for n in range(len(tok)):
+        b, h = seq[n], head[n]
+        i = tok[n] - cu_q[b]
+        Lq, Lk = cu_q[b + 1] - cu_q[b], cu_k[b + 1] - cu_k[b]
+        if Lk == 0:
+            continue
+        kk = k[cu_k[b]:cu_k[b + 1], h // g]
+        vv = np.abs(v[cu_k[b]:cu_k[b + 1], h // g])
+        pos = i + Lk - Lq
+        j = np.arange(Lk)
+        right = 0 if causal else wr
+        vis = np.ones(Lk, bool)
+        if right >= 0:
+            vis &= j <= pos + right
+        if wl >= 0:
+            vis &= j >= pos - wl
+        if not vis.any():
+            continue
+        x = scale * (kk[vis] @ q[tok[n], h]) / np.log(2.0)   # log2 units
+        ph = np.exp2(x - x.max())
+        L = ph.sum()
+        P = ph / L
+        va = vv[vis]
+        pv = P @ va
+        sub = np.where(ph < 2.0 ** -10, np.minimum(ph, 2.0 ** -14), 0.0) @ va / L
+        o = P @ (v[cu_k[b]:cu_k[b + 1], h // g][vis])
+        bound[n] = (2.0 ** -4 + 2.0 ** -12) * pv + sub + 2.0 ** -9 * np.abs(o)
+        sigma[n] = 2.0 ** -4 / np.sqrt(3.0) * np.sqrt((P ** 2) @ (va ** 2))
+    if rows is None:
+        bound = bound.reshape(tq, Hq, d)
+        sigma = sigma.reshape(tq, Hq, d)
+    return bound, sigma

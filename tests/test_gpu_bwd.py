@@ -94,3 +94,10 @@ def test_backward_is_deterministic(attn):
     torch.cuda.synchronize()
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+def test_backward_at_the_benchmarked_shape(attn):
+    """The causal B=4, H=16, N=4096, d=128 workload the benchmark times, with the benchmark's
+    seeded dout, against the full fp64 oracle gradients (about a minute on the host cores)."""
+    case = synth.config_case(2)
+    run_case(attn, case, 1200)
