@@ -4,11 +4,19 @@
 One step = one pass of the whole path over one batch: the causal prefill workload
 (B=4, Hq=Hkv=16, N=4096, d=128, packed varlen layout) through attn_fwd, then the paged decode
 workload (batch 64, cache lengths U[1024, 32768], page 256, Hq=32, Hkv=8, d=128) through
-attn_decode_kvcache.  Inputs are resident in HBM when the timed region starts and are larger
-than L2 (no flush).  The headline value is the prefill's TFLOPS; the decode's GB/s sits in
-"decode".  Both carry a roofline object against the measured peaks.
+attn_decode_kvcache.  Inputs are resident in HBM when the timed region starts.  The headline
+value is the prefill's TFLOPS; the decode's GB/s sits in "decode".  Both carry a roofline
+object against the measured peaks.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timing: W untimed steps, then K timed steps between a barrier and a device synchronisation;
+CUDA events on the launching stream bracket each call, and the reported times are the medians
+of the K per-call times (the mean can be pulled by one slow step).  The prefill inputs are
+larger than L2; before every decode call a 256 MiB buffer is read through so that the decode
+starts from a cold L2 (the read is outside the decode's events; a read leaves clean lines, so no
+write-back competes with the decode), and the single-head workload is timed the same way, one
+flushed call at a time.
 
 Under torchrun every rank runs its own replica of the workload (weak scaling, no collective
 on the data path); rank 0 prints one JSON line with the aggregate over ranks and the maximum
@@ -32,6 +40,20 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "prefill attn TFLOPS & decode KV GB/s on 1 GB300, % of roofline"
+L2_FLUSH_BYTES = 256 << 20  # twice the GB300's L2
+
+
+class L2Flush:
+    """Evicts L2 by reading a device buffer twice its size (a reduction kernel)."""
+
+    def __init__(self, device):
+        import torch
+        self.buf = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=device)
+        self.out = torch.empty((), dtype=torch.int64, device=device)
+
+    def __call__(self):
+        import torch
+        torch.sum(self.buf, dim=0, out=self.out)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PREFILL_CFG, DECODE_CFG = 2, 4
 
@@ -54,6 +76,13 @@ def reduce_max(values, world, device=None):
     t = torch.tensor(values, dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return t.tolist()
+
+
+def job_rate(units_per_rank, ms_per_rank, world):
+    """Whole-job throughput of `world` replicas that each process `units_per_rank` units: the
+    units of all ranks over the slowest rank's time (ms_per_rank already reduced to the max
+    over ranks), in units per second."""
+    return world * units_per_rank / (ms_per_rank * 1e-3)
 
 
 def load_peaks():
@@ -111,7 +140,7 @@ class ClockSampler:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                   "-lms", "50", "-f", self.path]
+                   "-lms", "10", "-f", self.path]
             self.proc = subprocess.Popen(cmd, stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -154,10 +183,12 @@ class ClockSampler:
 
 # ---- the CPU oracle (cpu_baseline and the reference arm) ------------------------------------
 
-def oracle_rate(case, seconds, seed=0):
-    """Time the fp64 oracle on seeded rows of a prefill case for about `seconds` of CPU work.
+def oracle_rate(case, seconds, seed=0, n_rows=None):
+    """Time the fp64 oracle on seeded rows of a prefill case for about `seconds` of CPU work
+    (or on exactly `n_rows` rows, skipping the calibration).
 
-    Returns (TFLOPS-equivalent, threads, sample description, seconds taken, flops done)."""
+    Returns (TFLOPS-equivalent, threads, sample description, seconds taken, flops done,
+    rows)."""
     import numpy as np
     import torch
     from oracle import oracle
@@ -181,8 +212,8 @@ def oracle_rate(case, seconds, seed=0):
 
     # calibrate on a small sample and then on one of about a second (fixed costs dominate the
     # first), then run a sample sized for `seconds`
-    n = 32
-    for target in (1.0, seconds):
+    n = 32 if n_rows is None else n_rows
+    for target in ((1.0, seconds) if n_rows is None else ()):
         t, h = rows(n)
         t0 = time.perf_counter()
         oracle.attn_fwd_rows(case.q, case.k, case.v, case.cu_seqlens_q, case.cu_seqlens_k,
@@ -197,10 +228,163 @@ def oracle_rate(case, seconds, seed=0):
                          case.window_right)
     dt = time.perf_counter() - t0
     fl = sum(4 * d * pairs_of_row(x) for x in t.tolist())
-    return fl / dt / 1e12, oracle.num_threads(), f"{n} seeded (token, head) rows", dt, fl
+    return fl / dt / 1e12, oracle.num_threads(), f"{n} seeded (token, head) rows", dt, fl, n
 
 
 # ---- our implementation ---------------------------------------------------------------------
+
+def median_ms(fn, stream, reps=30, warm=10, flush=None):
+    """Median over `reps` calls of fn's CUDA-event time on `stream`, after `warm` untimed calls;
+    with `flush` (an L2Flush) L2 is evicted before every call, outside the events."""
+    import torch
+    for _ in range(warm):
+        fn()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for a, b in ev:
+        if flush is not None:
+            flush()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+
+EXTRA_WORKLOADS = ("cfg1", "cfg3", "cfg5", "chunked", "mods", "bwd", "fp8")
+
+
+def build_workload(name, dev):
+    """One of the extra workloads, its inputs on the device: a dict with the call, its
+    algorithmic work (FLOP, or bytes), the rate's unit ("tflops": work / ms / 1e9), a
+    description and whether the call is timed from a cold L2."""
+    import torch
+    from exact_attention_70_gb300 import binding, synth, workload
+    if name in ("cfg1", "cfg2", "cfg3", "cfg5"):
+        c = synth.config_case(int(name[3:]))
+        q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+        cq, ck = c.cu_seqlens_q.to(dev), c.cu_seqlens_k.to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=dev)
+        ws = torch.empty(binding.attn_fwd_workspace_bytes(c.batch, c.max_seqlen_q, q.shape[1],
+                                                          k.shape[1]), dtype=torch.uint8,
+                         device=dev)
+
+        def call():
+            binding.attn_fwd(q, k, v, cq, ck, c.max_seqlen_q, c.max_seqlen_k, c.softmax_scale,
+                             c.causal, c.window_left, c.window_right, out=o, lse=lse,
+                             workspace=ws)
+        # the single-head workload fits in L2: it is timed from a cold L2, call by call
+        return dict(call=call, work=workload.prefill_case_flops(c), unit="tflops",
+                    desc=synth.CONFIG_NAMES[int(name[3:])], flush=name == "cfg1")
+    if name == "chunked":
+        # chunked prefill against the paged cache (append + rotary + attention, one call)
+        c = synth.chunked_case()
+        t = {f: getattr(c, f).to(dev) for f in ("q", "k_new", "v_new", "k_cache", "v_cache",
+                                                 "cache_seqlens", "block_table", "cu_seqlens_q",
+                                                 "rotary_cos", "rotary_sin")}
+        o = torch.empty_like(t["q"])
+        lse = torch.empty((t["q"].shape[1], t["q"].shape[0]), dtype=torch.float32, device=dev)
+
+        def call():
+            binding.attn_fwd_kvcache(t["q"], t["k_new"], t["v_new"], t["k_cache"], t["v_cache"],
+                                     t["cache_seqlens"], t["block_table"], t["cu_seqlens_q"],
+                                     c.max_seqlen_q, c.softmax_scale, c.causal, -1, -1,
+                                     t["rotary_cos"], t["rotary_sin"], False, out=o, lse=lse)
+        ql = (c.cu_seqlens_q[1:] - c.cu_seqlens_q[:-1]).tolist()
+        lk = [int(x) + n for x, n in zip(c.cache_seqlens.tolist(), ql)]
+        return dict(call=call, unit="tflops", desc=synth.CHUNKED_NAME, flush=False,
+                    work=workload.prefill_flops(ql, lk, t["q"].shape[1], t["q"].shape[2], True))
+    if name == "mods":
+        # the causal prefill workload with both score modifiers (softcap 30, ALiBi slopes)
+        c = synth.config_case(2)
+        q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+        cq, ck = c.cu_seqlens_q.to(dev), c.cu_seqlens_k.to(dev)
+        Hq = q.shape[1]
+        slopes = torch.tensor([2.0 ** (-8.0 * (h + 1) / Hq) for h in range(Hq)],
+                              dtype=torch.float32, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((Hq, q.shape[0]), dtype=torch.float32, device=dev)
+
+        def call():
+            binding.attn_fwd_mods(q, k, v, cq, ck, c.max_seqlen_q, c.max_seqlen_k,
+                                  c.softmax_scale, True, softcap=30.0, alibi_slopes=slopes,
+                                  out=o, lse=lse)
+        return dict(call=call, work=workload.prefill_case_flops(c), unit="tflops", flush=False,
+                    desc=synth.CONFIG_NAMES[2] + " with softcap 30 and ALiBi")
+    if name == "bwd":
+        # backward of the causal prefill workload (gradients of q, k, v)
+        c = synth.config_case(2)
+        q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+        cq, ck = c.cu_seqlens_q.to(dev), c.cu_seqlens_k.to(dev)
+        o, lse = binding.attn_fwd(q, k, v, cq, ck, c.max_seqlen_q, c.max_seqlen_k,
+                                  c.softmax_scale, True)
+        do = synth.randn_bf16(tuple(c.q.shape), 1200, 9).to(dev)
+        gq, gk, gv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(binding.attn_bwd_workspace_bytes(q.shape[0], q.shape[1]),
+                         dtype=torch.uint8, device=dev)
+
+        def call():
+            binding.attn_bwd(q, k, v, o, do, lse, cq, ck, c.max_seqlen_q, c.max_seqlen_k,
+                             c.softmax_scale, True, dq=gq, dk=gk, dv=gv, workspace=ws)
+        # S, dP, dV, dK, dQ: 10 d per visible pair
+        return dict(call=call, work=workload.prefill_case_flops(c) * 10 // 4, unit="tflops",
+                    desc="backward of " + synth.CONFIG_NAMES[2], flush=False)
+    if name in ("fp8", "quant"):
+        # the causal prefill workload's shape with FP8 e4m3 inputs and block scales, and the
+        # quantizer that produces such inputs from bf16 (rotation of Q and K on)
+        c = synth.fp8_bench_case()
+        f8 = [x.to(dev) for x in (c.q8, c.k8, c.v8t, c.q_scale, c.k_scale, c.v_scale,
+                                  c.cu_seqlens_q, c.cu_seqlens_k)]
+        o = torch.empty((c.q8.shape[0], c.q8.shape[1], c.q8.shape[2]), dtype=torch.bfloat16,
+                        device=dev)
+        lse = torch.empty((c.q8.shape[1], c.q8.shape[0]), dtype=torch.float32, device=dev)
+        cq_ = synth.config_case(2)
+        bq, bk, bv = cq_.q.to(dev), cq_.k.to(dev), cq_.v.to(dev)
+        bck = cq_.cu_seqlens_k.to(dev)
+        sg = torch.where(torch.arange(128, device=dev) % 3 == 0, -1.0, 1.0).float()
+
+        def call():
+            binding.attn_fwd_fp8(*f8, c.max_seqlen_q, c.max_seqlen_k, c.softmax_scale,
+                                 c.causal, out=o, lse=lse)
+
+        def quant():
+            binding.attn_quantize_fp8(bq, bk, bv, bck, cq_.max_seqlen_k, signs=sg)
+        # bytes: Q, K, V read as bf16 (V twice: its maximum, then its codes), codes written
+        qbytes = (bq.numel() + bk.numel() + 2 * bv.numel()) * 2 + bq.numel() + bk.numel() + bv.numel()
+        if name == "quant":
+            return dict(call=quant, work=qbytes, unit="gbs", flush=False,
+                        desc="FP8 quantizer on " + synth.CONFIG_NAMES[2])
+        ql = (c.cu_seqlens_q[1:] - c.cu_seqlens_q[:-1]).tolist()
+
+        def after(stream):
+            qms = median_ms(quant, stream)
+            return {"quantize_ms": round(qms, 4), "quantize_gbs": round(qbytes / qms / 1e6, 1)}
+        return dict(call=call, unit="tflops", desc=synth.FP8_NAME, flush=False, after=after,
+                    work=workload.prefill_flops(ql, ql, c.q8.shape[1], c.q8.shape[2], c.causal))
+    raise ValueError(name)
+
+
+def run_workload(args):
+    """--workload NAME: only that workload, W untimed and K timed calls (profiler captures)."""
+    import torch
+    from exact_attention_70_gb300 import binding
+    from exact_attention_70_gb300 import build as attn_build
+    torch.cuda.set_device(0)
+    attn_build.build()
+    binding.load()
+    dev = torch.device("cuda", 0)
+    w = build_workload(args.workload, dev)
+    stream = torch.cuda.current_stream()
+    flush = L2Flush(dev) if w["flush"] else None
+    ms = median_ms(w["call"], stream, reps=args.steps, warm=args.warmup, flush=flush)
+    if binding.attn_get_device_status() != 0:
+        raise RuntimeError("device status is not ok")
+    print(json.dumps({"workload": w["desc"], "ms": round(ms, 4),
+                      w["unit"]: round(w["work"] / ms / 1e9, 2), "steps": args.steps,
+                      "warmup": args.warmup}))
+
+
 
 def run_ours(args, rank, world, local):
     import torch
@@ -271,15 +455,18 @@ def run_ours(args, rank, world, local):
         binding.attn_decode_kvcache(dq, kc, vc, sl, bt, dec.softmax_scale, 0, out=dout,
                                     lse=dlse, workspace=ws_d)
 
+    flush = L2Flush(dev)
+
     for _ in range(args.warmup):
         prefill()
+        flush()
         decode()
     torch.cuda.synchronize()
     if binding.attn_get_device_status() != 0:
         raise RuntimeError("device status after warm-up is not ok")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     if world > 1:
@@ -292,8 +479,10 @@ def run_ours(args, rank, world, local):
         ev[i][0].record(stream)
         prefill()
         ev[i][1].record(stream)
-        decode()
+        flush()  # cold L2 for the decode
         ev[i][2].record(stream)
+        decode()
+        ev[i][3].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -301,8 +490,8 @@ def run_ours(args, rank, world, local):
     clk = clocks.stop()
     status = binding.attn_get_device_status()
     total_ms = t_start.elapsed_time(t_end)
-    pre_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    dec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    pre_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    dec_ms = statistics.median(e[2].elapsed_time(e[3]) for e in ev)
     total_ms, pre_ms, dec_ms = reduce_max([total_ms, pre_ms, dec_ms], world, dev)
 
     # end to end through the public API: pinned host inputs in, results back to the host
@@ -373,7 +562,7 @@ def run_ours(args, rank, world, local):
         h_dlse.copy_(dlse, non_blocking=True)
         pe[i][1].record(stream)
     torch.cuda.synchronize()
-    e2e_dec = statistics.mean(e[0].elapsed_time(e[1]) for e in pe[2:])
+    e2e_dec = statistics.median(e[0].elapsed_time(e[1]) for e in pe[2:])
     e2e_pre, e2e_dec = reduce_max([e2e_pre, e2e_dec], world, dev)
     h2d_pre = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_cuq, h_cuk))
     d2h_pre = out.numel() * 2 + lse.numel() * 4
@@ -383,165 +572,14 @@ def run_ours(args, rank, world, local):
     # the other workloads, timed alone (parity cases; reported for context)
     extra = {}
     if not args.no_extra:
-        for cfg in (1, 3, 5):
-            c = synth.config_case(cfg)
-            cq, ck, cv = c.q.to(dev), c.k.to(dev), c.v.to(dev)
-            ccq, cck = c.cu_seqlens_q.to(dev), c.cu_seqlens_k.to(dev)
-            co = torch.empty_like(cq)
-            cl = torch.empty((cq.shape[1], cq.shape[0]), dtype=torch.float32, device=dev)
-            cws = torch.empty(binding.attn_fwd_workspace_bytes(c.batch, c.max_seqlen_q,
-                                                               cq.shape[1], ck.shape[1]),
-                              dtype=torch.uint8, device=dev)
-
-            def run_c():
-                binding.attn_fwd(cq, ck, cv, ccq, cck, c.max_seqlen_q, c.max_seqlen_k,
-                                 c.softmax_scale, c.causal, c.window_left, c.window_right,
-                                 out=co, lse=cl, workspace=cws)
-            for _ in range(5):
-                run_c()
-            reps = 20
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for _ in range(reps):
-                run_c()
-            b.record(stream)
-            torch.cuda.synchronize()
-            ms = a.elapsed_time(b) / reps
-            fl = workload.prefill_case_flops(c)
-            extra[f"cfg{cfg}"] = {"workload": synth.CONFIG_NAMES[cfg], "ms": round(ms, 4),
-                                  "tflops": round(fl / ms / 1e9, 2)}
-            del cq, ck, cv, co
-        # chunked prefill against the paged cache (append + rotary + attention, one call)
-        c = synth.chunked_case()
-        t = {f: getattr(c, f) for f in ("q", "k_new", "v_new", "k_cache", "v_cache",
-                                        "cache_seqlens", "block_table", "cu_seqlens_q",
-                                        "rotary_cos", "rotary_sin")}
-        t = {f: x.to(dev) for f, x in t.items()}
-        co = torch.empty_like(t["q"])
-        cl = torch.empty((t["q"].shape[1], t["q"].shape[0]), dtype=torch.float32, device=dev)
-
-        def run_k():
-            binding.attn_fwd_kvcache(t["q"], t["k_new"], t["v_new"], t["k_cache"], t["v_cache"],
-                                     t["cache_seqlens"], t["block_table"], t["cu_seqlens_q"],
-                                     c.max_seqlen_q, c.softmax_scale, c.causal, -1, -1,
-                                     t["rotary_cos"], t["rotary_sin"], False, out=co, lse=cl)
-        for _ in range(5):
-            run_k()
-        reps = 20
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(reps):
-            run_k()
-        b.record(stream)
-        torch.cuda.synchronize()
-        ms = a.elapsed_time(b) / reps
-        ql = (c.cu_seqlens_q[1:] - c.cu_seqlens_q[:-1]).tolist()
-        lk = [int(x) + n for x, n in zip(c.cache_seqlens.tolist(), ql)]
-        fl = workload.prefill_flops(ql, lk, t["q"].shape[1], t["q"].shape[2], True)
-        extra["chunked"] = {"workload": synth.CHUNKED_NAME, "ms": round(ms, 4),
-                            "tflops": round(fl / ms / 1e9, 2)}
-        del t, co
-        # the causal prefill workload with both score modifiers (softcap 30, ALiBi slopes)
-        c = synth.config_case(2)
-        mq, mk, mv = c.q.to(dev), c.k.to(dev), c.v.to(dev)
-        mcq, mck = c.cu_seqlens_q.to(dev), c.cu_seqlens_k.to(dev)
-        Hq = mq.shape[1]
-        slopes = torch.tensor([2.0 ** (-8.0 * (h + 1) / Hq) for h in range(Hq)],
-                              dtype=torch.float32, device=dev)
-        mo, ml = torch.empty_like(mq), torch.empty((Hq, mq.shape[0]), dtype=torch.float32, device=dev)
-
-        def run_m():
-            binding.attn_fwd_mods(mq, mk, mv, mcq, mck, c.max_seqlen_q, c.max_seqlen_k,
-                                  c.softmax_scale, True, softcap=30.0, alibi_slopes=slopes,
-                                  out=mo, lse=ml)
-        for _ in range(3):
-            run_m()
-        reps = 10
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(reps):
-            run_m()
-        b.record(stream)
-        torch.cuda.synchronize()
-        ms = a.elapsed_time(b) / reps
-        extra["mods"] = {"workload": synth.CONFIG_NAMES[2] + " with softcap 30 and ALiBi",
-                         "ms": round(ms, 4),
-                         "tflops": round(workload.prefill_case_flops(c) / ms / 1e9, 2)}
-        del mq, mk, mv, mo
-        # backward of the causal prefill workload (gradients of q, k, v)
-        c = synth.config_case(2)
-        bq, bk, bv = c.q.to(dev), c.k.to(dev), c.v.to(dev)
-        bcq, bck = c.cu_seqlens_q.to(dev), c.cu_seqlens_k.to(dev)
-        bo, bl = binding.attn_fwd(bq, bk, bv, bcq, bck, c.max_seqlen_q, c.max_seqlen_k,
-                                  c.softmax_scale, True)
-        bdo = synth.randn_bf16(tuple(c.q.shape), 1200, 9).to(dev)
-        gq, gk, gv = torch.empty_like(bq), torch.empty_like(bk), torch.empty_like(bv)
-        bws = torch.empty(binding.attn_bwd_workspace_bytes(bq.shape[0], bq.shape[1]),
-                          dtype=torch.uint8, device=dev)
-
-        def run_b():
-            binding.attn_bwd(bq, bk, bv, bo, bdo, bl, bcq, bck, c.max_seqlen_q, c.max_seqlen_k,
-                             c.softmax_scale, True, dq=gq, dk=gk, dv=gv, workspace=bws)
-        for _ in range(3):
-            run_b()
-        reps = 10
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(reps):
-            run_b()
-        b.record(stream)
-        torch.cuda.synchronize()
-        ms = a.elapsed_time(b) / reps
-        fl = workload.prefill_case_flops(c) * 10 // 4   # S, dP, dV, dK, dQ: 10 d per pair
-        extra["bwd"] = {"workload": "backward of " + synth.CONFIG_NAMES[2], "ms": round(ms, 4),
-                        "tflops": round(fl / ms / 1e9, 2)}
-        del bq, bk, bv, bo, bdo, gq, gk, gv
-        # the causal prefill workload's shape with FP8 e4m3 inputs and block scales
-        c = synth.fp8_bench_case()
-        f8 = [x.to(dev) for x in (c.q8, c.k8, c.v8t, c.q_scale, c.k_scale, c.v_scale,
-                                  c.cu_seqlens_q, c.cu_seqlens_k)]
-        fo = torch.empty((c.q8.shape[0], c.q8.shape[1], c.q8.shape[2]), dtype=torch.bfloat16,
-                         device=dev)
-        fl_ = torch.empty((c.q8.shape[1], c.q8.shape[0]), dtype=torch.float32, device=dev)
-
-        def run_f():
-            binding.attn_fwd_fp8(*f8, c.max_seqlen_q, c.max_seqlen_k, c.softmax_scale, c.causal,
-                                 out=fo, lse=fl_)
-        for _ in range(5):
-            run_f()
-        reps = 20
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(reps):
-            run_f()
-        b.record(stream)
-        torch.cuda.synchronize()
-        ms = a.elapsed_time(b) / reps
-        ql = (c.cu_seqlens_q[1:] - c.cu_seqlens_q[:-1]).tolist()
-        fl = workload.prefill_flops(ql, ql, c.q8.shape[1], c.q8.shape[2], c.causal)
-        # and the quantizer that produces such inputs from bf16 (rotation of Q and K on)
-        cq_ = synth.config_case(2)
-        bq_, bk_, bv_ = cq_.q.to(dev), cq_.k.to(dev), cq_.v.to(dev)
-        bck_ = cq_.cu_seqlens_k.to(dev)
-        sg_ = torch.where(torch.arange(128, device=dev) % 3 == 0, -1.0, 1.0).float()
-
-        def run_qz():
-            binding.attn_quantize_fp8(bq_, bk_, bv_, bck_, cq_.max_seqlen_k, signs=sg_)
-        for _ in range(3):
-            run_qz()
-        a.record(stream)
-        for _ in range(reps):
-            run_qz()
-        b.record(stream)
-        torch.cuda.synchronize()
-        qms = a.elapsed_time(b) / reps
-        # bytes: Q, K, V read as bf16 (V twice: its maximum, then its codes), codes written
-        qbytes = (bq_.numel() + bk_.numel() + 2 * bv_.numel()) * 2 + bq_.numel() + bk_.numel() + bv_.numel()
-        extra["fp8"] = {"workload": synth.FP8_NAME, "ms": round(ms, 4),
-                        "tflops": round(fl / ms / 1e9, 2),
-                        "quantize_ms": round(qms, 4),
-                        "quantize_gbs": round(qbytes / qms / 1e6, 1)}
-        del f8, fo, fl_, bq_, bk_, bv_
+        for name in EXTRA_WORKLOADS:
+            w = build_workload(name, dev)
+            ms = median_ms(w["call"], stream, flush=flush if w["flush"] else None)
+            extra[name] = {"workload": w["desc"], "ms": round(ms, 4),
+                           w["unit"]: round(w["work"] / ms / 1e9, 2)}
+            if "after" in w:
+                extra[name].update(w["after"](stream))
+            del w
     return dict(p_flops=p_flops, d_bytes=d_bytes, total_ms=total_ms, pre_ms=pre_ms,
                 dec_ms=dec_ms, e2e_pre=e2e_pre, e2e_dec=e2e_dec, h2d_pre=h2d_pre,
                 d2h_pre=d2h_pre, h2d_dec=h2d_dec, d2h_dec=d2h_dec, clocks=clk, splits=splits,
@@ -551,8 +589,8 @@ def run_ours(args, rank, world, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -561,7 +599,14 @@ def main():
                     help="time one half of the step only (for profiler captures)")
     ap.add_argument("--decode-batch", type=int, default=64,
                     help="use the first B sequences of the decode workload (profiling)")
+    ap.add_argument("--workload", choices=["step", "cfg1", "cfg2", "cfg3", "cfg5", "chunked",
+                                           "mods", "bwd", "fp8", "quant"], default="step",
+                    help="run one workload alone, W + K calls, instead of the timed step "
+                         "(for profiler captures; prints that workload's median time only)")
     args = ap.parse_args()
+    if args.workload != "step":
+        run_workload(args)
+        return
     rank, world, local = dist_env()
     peaks, peak_src = load_peaks()
 
@@ -570,16 +615,19 @@ def main():
             return
         from exact_attention_70_gb300 import synth
         case = synth.config_case(PREFILL_CFG)
-        budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+        # every step runs the same number of rows, sized once so that the W + K steps take
+        # about 90 s of host time together
+        budget = max(0.2, 90.0 / max(1, args.steps + args.warmup))
+        _, _, _, _, _, n_rows = oracle_rate(case, budget, seed=10 ** 6)
         rates, times = [], []
         for i in range(args.warmup + args.steps):
-            r, cores, sample, dt, _ = oracle_rate(case, budget, seed=i)
+            r, cores, sample, dt, _, _ = oracle_rate(case, budget, seed=i, n_rows=n_rows)
             if i >= args.warmup:
                 rates.append(r)
                 times.append(dt * 1e3)
-        value = statistics.mean(rates)
+        value = statistics.median(rates)
         line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(times),
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.median(times),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "impl": "reference",
                 "config": {"workload": synth.CONFIG_NAMES[PREFILL_CFG], "sample": sample},
@@ -596,8 +644,8 @@ def main():
     if args.only == "prefill":
         r["d_bytes"], r["e2e_dec"] = 0, max(r["e2e_dec"], 1e-9)
     r["pre_ms"], r["dec_ms"] = max(r["pre_ms"], 1e-9), max(r["dec_ms"], 1e-9)
-    pre_tflops = world * r["p_flops"] / (r["pre_ms"] * 1e-3) / 1e12
-    dec_gbs = world * r["d_bytes"] / (r["dec_ms"] * 1e-3) / 1e9
+    pre_tflops = job_rate(r["p_flops"], r["pre_ms"], world) / 1e12
+    dec_gbs = job_rate(r["d_bytes"], r["dec_ms"], world) / 1e9
     tensor_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     per_gpu_pre = r["p_flops"] / (r["pre_ms"] * 1e-3) / 1e12
@@ -606,7 +654,7 @@ def main():
         return
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        rate, cores, sample, dt, fl = oracle_rate(r["pre"], args.cpu_seconds)
+        rate, cores, sample, dt, fl, _ = oracle_rate(r["pre"], args.cpu_seconds)
         cpu = {"value": rate, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
                "sample": f"{sample} of the prefill workload, {dt:.1f} s, {fl:.3e} FLOP"}
     launches_per_step = (2 if args.only != "decode" else 0) + (
@@ -629,7 +677,8 @@ def main():
             "prefill_flops_per_step": r["p_flops"],
             "decode_bytes_per_step": r["d_bytes"],
             "decode_num_splits": r["splits"],
-            "l2": "inputs larger than L2 (no flush)",
+            "l2": "prefill inputs larger than L2; 256 MiB read through before each decode call",
+            "timing": "median of the timed steps' per-call CUDA-event times",
             "parallelism": f"replicas x{world}",
         },
         "roofline": {
@@ -649,13 +698,13 @@ def main():
                 "kernel": "decode_split_kernel + combine (CUDA events around attn_decode_kvcache)",
                 "peak_source": f"{peak_src} copy bandwidth",
             },
-            "e2e": {"value": round(world * r["d_bytes"] / (r["e2e_dec"] * 1e-3) / 1e9, 2),
+            "e2e": {"value": round(job_rate(r["d_bytes"], r["e2e_dec"], world) / 1e9, 2),
                     "unit": "GB/s", "h2d_bytes_per_step": r["h2d_dec"],
                     "d2h_bytes_per_step": r["d2h_dec"],
                     "note": "KV cache resident in HBM; new queries and tables copied in"},
         },
         "prefill_ms": round(r["pre_ms"], 5),
-        "e2e": {"value": round(world * r["p_flops"] / (r["e2e_pre"] * 1e-3) / 1e12, 3),
+        "e2e": {"value": round(job_rate(r["p_flops"], r["e2e_pre"], world) / 1e12, 3),
                 "unit": "TFLOPS", "h2d_bytes_per_step": r["h2d_pre"],
                 "d2h_bytes_per_step": r["d2h_pre"],
                 "note": "each step copies its inputs in and its results out; copies run on "

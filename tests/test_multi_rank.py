@@ -31,30 +31,38 @@ def _worker(rank, world, port, q):
         times = [10.0 + rank, 3.0 * (1 + rank), 5.0 - rank]
         dist.barrier()
         got = bench.reduce_max(times, world)
-        q.put((rank, got))
+        # the job's rate: each rank processed the same units; rank 1 is the slower one on the
+        # first time, so the aggregate is twice the units over rank 1's time
+        units = 274945015808
+        rate = bench.job_rate(units, got[0], world)
+        own = bench.job_rate(units, times[0], world)
+        q.put((rank, got, rate, own))
     finally:
         dist.destroy_process_group()
 
 
-def test_two_gloo_ranks_agree_on_max_times():
+def test_two_gloo_ranks_agree_on_max_times_and_the_job_rate():
     world, port = 2, _free_port()
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
     for p in procs:
         p.start()
-    results = dict(q.get(timeout=120) for _ in range(world))
+    results = {r: (got, rate, own) for r, got, rate, own in (q.get(timeout=120) for _ in range(world))}
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
     expect = [11.0, 6.0, 5.0]
-    assert results[0] == expect and results[1] == expect
+    assert results[0][0] == expect and results[1][0] == expect
+    # both ranks report the same job rate, set by the slowest rank's 11 ms
+    assert results[0][1] == results[1][1] == 2 * 274945015808 / 11e-3
+    # rank 0 alone was faster (10 ms): the aggregate must not use its own time
+    assert results[0][1] < results[0][2]
 
 
-def test_weak_scaling_value_is_units_of_all_ranks_over_slowest_time():
+def test_job_rate_is_units_of_all_ranks_over_slowest_time():
     import bench
-    # 2 replicas of 2.7495e11 FLOP each, slowest rank 0.36 ms -> aggregate TFLOPS
-    flops, ms, world = 274945015808, 0.36, 2
-    assert bench.reduce_max([ms], 1) == [ms]
-    value = world * flops / (ms * 1e-3) / 1e12
-    assert abs(value - 1527.47) < 0.01
+    # one replica: the rate is just units over time; N replicas multiply the units, not the time
+    assert bench.job_rate(1000, 2.0, 1) == 1000 / 2e-3
+    assert bench.job_rate(1000, 2.0, 4) == 4 * bench.job_rate(1000, 2.0, 1)
+    assert bench.reduce_max([2.0, 3.0], 1) == [2.0, 3.0]
