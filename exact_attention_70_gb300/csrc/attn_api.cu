@@ -6,6 +6,7 @@
 
 #include <math.h>
 #include <mutex>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -59,6 +60,13 @@ attn_status_t device_state(DeviceState** out) {
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// An NVTX range around each computing entry point, so that profiler timelines show the C-ABI
+// calls by name (NVTX is header-only and costs next to nothing without a tool attached).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
 
 // 3-D bf16 tensor [n2][n1][n0] (n0 contiguous), 128-byte swizzled boxes {64, b1, b2}.
 attn_status_t encode_3d(CUtensorMap* map, const void* base, uint64_t n0, uint64_t n1,
@@ -260,6 +268,7 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* out, f
                        int nheads_q, int nheads_kv, int head_dim, float softmax_scale,
                        int causal, int window_left, int window_right, void* workspace,
                        size_t workspace_bytes, void* stream) {
+    NvtxRange nvtx_range("attn_fwd");
     return fwd_impl(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
                     max_seqlen_q, max_seqlen_k, nheads_q, nheads_kv, head_dim, softmax_scale,
                     causal, window_left, window_right, workspace, workspace_bytes, stream, 0.f,
@@ -273,6 +282,7 @@ attn_status_t attn_fwd_mods(const void* q, const void* k, const void* v, void* o
                             int causal, int window_left, int window_right, float softcap,
                             const float* alibi_slopes, void* workspace, size_t workspace_bytes,
                             void* stream) {
+    NvtxRange nvtx_range("attn_fwd_mods");
     return fwd_impl(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
                     max_seqlen_q, max_seqlen_k, nheads_q, nheads_kv, head_dim, softmax_scale,
                     causal, window_left, window_right, workspace, workspace_bytes, stream,
@@ -286,6 +296,7 @@ attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
                            int max_seqlen_q, int max_seqlen_k, int nheads_q, int nheads_kv,
                            int head_dim, int key_blocks, float softmax_scale, int causal,
                            int window_left, int window_right, void* stream) {
+    NvtxRange nvtx_range("attn_fwd_fp8");
     if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
         nheads_q <= 0 || nheads_kv <= 0 || key_blocks < 0 || window_left < -1 ||
         window_right < -1 || !scale_ok(softmax_scale))
@@ -352,6 +363,7 @@ attn_status_t attn_quantize_fp8(const void* q, const void* k, const void* v,
                                 int key_blocks, const float* signs, void* q8, float* q_scale,
                                 void* k8, float* k_scale, void* v8t, float* v_scale,
                                 void* stream) {
+    NvtxRange nvtx_range("attn_quantize_fp8");
     if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_k < 0 || nheads_q <= 0 ||
         nheads_kv <= 0 || key_blocks < 0)
         return ATTN_ERR_INVALID_ARG;
@@ -414,6 +426,7 @@ attn_status_t attn_fwd_kvcache(const void* q, const void* k_new, const void* v_n
                                int max_pages_per_seq, int num_pages, float softmax_scale,
                                int causal, int window_left, int window_right, void* workspace,
                                size_t workspace_bytes, void* stream) {
+    NvtxRange nvtx_range("attn_fwd_kvcache");
     if (batch < 0 || total_q < 0 || max_seqlen_q < 0 || nheads_q <= 0 || nheads_kv <= 0 ||
         window_left < -1 || window_right < -1 || !scale_ok(softmax_scale) ||
         max_pages_per_seq <= 0 || num_pages <= 0 || page_size <= 0)
@@ -561,6 +574,7 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        int nheads_q, int nheads_kv, int head_dim, float softmax_scale,
                        int causal, int window_left, int window_right, void* workspace,
                        size_t workspace_bytes, void* stream) {
+    NvtxRange nvtx_range("attn_bwd");
     if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
         nheads_q <= 0 || nheads_kv <= 0 || window_left < -1 || window_right < -1 ||
         !scale_ok(softmax_scale))
@@ -663,6 +677,7 @@ attn_status_t attn_decode_kvcache(const void* q, const void* k_cache, const void
                                   int batch, int nheads_q, int nheads_kv, int head_dim,
                                   int max_pages_per_seq, int num_pages, float softmax_scale,
                                   void* workspace, size_t workspace_bytes, void* stream) {
+    NvtxRange nvtx_range("attn_decode_kvcache");
     if (batch < 0 || nheads_q <= 0 || nheads_kv <= 0 || nheads_q % nheads_kv != 0 ||
         max_pages_per_seq < 0 || num_pages < 0 || num_splits < 0 || num_splits > 64 ||
         page_size <= 0 || !scale_ok(softmax_scale))

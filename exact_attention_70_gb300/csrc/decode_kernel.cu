@@ -315,6 +315,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
             const float lse = lsum > 0.f ? (M + __log2f(lsum)) * kLn2f : -INFINITY;
             const int head = kvh * p.g + hg * kDecRowsPerCta + r;
             const size_t bh = static_cast<size_t>(b) * p.Hq + head;
+            if (!ATTN_IN_BOUNDS(head < p.Hq && b < p.batch, p.status)) continue;
             if (S == 1) {
                 p.out[bh * D + d] = __float2bfloat16_rn(out);
                 if (d == 0) p.lse[bh] = lse;

@@ -360,6 +360,7 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
         const float vs = p.v_scale[static_cast<size_t>(b) * p.Hkv + kvh];
         const float mul = l > 0.f ? vs / l : 0.f;
         __nv_bfloat16* dst = p.out + (static_cast<size_t>(q0 + tok) * p.Hq + head) * 128;
+        const bool stored = ATTN_IN_BOUNDS(!valid || (q0 + tok < p.total_q && head < p.Hq), p.status);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             uint32_t o[32];
@@ -370,7 +371,7 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
 #pragma unroll
                 for (int e = 0; e < 32; ++e) o[e] = 0u;
             }
-            if (valid && ok) {
+            if (valid && ok && stored) {
                 uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * q);
 #pragma unroll
                 for (int v = 0; v < 4; ++v)
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
                         pack_bf16x2(__uint_as_float(o[8 * v + 6]) * mul, __uint_as_float(o[8 * v + 7]) * mul));
             }
         }
-        if (valid && ok)
+        if (valid && ok && stored)
             p.lse[static_cast<size_t>(head) * p.total_q + q0 + tok] =
                 l > 0.f ? (m_used + log2f(l) - kPLog2) * 0.69314718055994531f : -INFINITY;
     }

@@ -725,10 +725,14 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
                 if (k == 0) {
                     if (!__all_sync(0xffffffffu, wd.wait(epi_full, epi_cnt & 1))) return;
                     if (lane == 0) {
+                        if (ATTN_IN_BOUNDS(it.q0 + tv.tok0 >= 0 && it.q0 + tv.tok0 + p.tpt <= p.total_q &&
+                                               (it.kvh + 1) * g <= p.Hq,
+                                           p.status)) {
 #pragma unroll
-                        for (int h = 0; h < C::kHalves; ++h)
-                            tma_store_3d(&p.tm_o, smem + C::kOffP + t * C::kPTile + h * C::kAtomBytes,
-                                         h * 64, it.kvh * g, it.q0 + tv.tok0);
+                            for (int h = 0; h < C::kHalves; ++h)
+                                tma_store_3d(&p.tm_o, smem + C::kOffP + t * C::kPTile + h * C::kAtomBytes,
+                                             h * 64, it.kvh * g, it.q0 + tv.tok0);
+                        }
                         bulk_commit_group();
                     }
                 }
@@ -751,7 +755,8 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
                         const int head = it.kvh * g + (r - rt * g);
                         uint4* dst = reinterpret_cast<uint4*>(
                             p.out + (static_cast<size_t>(it.q0 + tok) * p.Hq + head) * D);
-                        dst[u] = ld_shared_v4(sw128_unit(p_tile, r, u));
+                        if (ATTN_IN_BOUNDS(it.q0 + tok < p.total_q && head < p.Hq, p.status))
+                            dst[u] = ld_shared_v4(sw128_unit(p_tile, r, u));
                     }
                 }
             } else {
@@ -766,10 +771,12 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
                     const int head = it.kvh * g + r % g;
                     uint4* dst = reinterpret_cast<uint4*>(
                         p.out + (static_cast<size_t>(it.q0 + tok) * p.Hq + head) * D);
+                    if (ATTN_IN_BOUNDS(it.q0 + tok < p.total_q && head < p.Hq, p.status)) {
 #pragma unroll
-                    for (int v = 0; v < kUnits; ++v) {
-                        const int u = (lane & 1) * kUnits + v;
-                        dst[u] = ld_shared_v4(sw128_unit(p_tile, r, u));
+                        for (int v = 0; v < kUnits; ++v) {
+                            const int u = (lane & 1) * kUnits + v;
+                            dst[u] = ld_shared_v4(sw128_unit(p_tile, r, u));
+                        }
                     }
                 }
             }
@@ -784,8 +791,10 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
                 if (r < tile_rows && tok < it.Lq) {
                     uint4* dst = reinterpret_cast<uint4*>(
                         p.out + (static_cast<size_t>(it.q0 + tok) * p.Hq + it.kvh * g + r % g) * D);
+                    if (ATTN_IN_BOUNDS(it.q0 + tok < p.total_q && it.kvh * g + r % g < p.Hq, p.status)) {
 #pragma unroll
-                    for (int v = 0; v < D / 32; ++v) dst[(lane & 3) * (D / 32) + v] = z;
+                        for (int v = 0; v < D / 32; ++v) dst[(lane & 3) * (D / 32) + v] = z;
+                    }
                 }
             }
         }
@@ -793,10 +802,10 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
         const bool valid_a = ra < tile_rows && tok_a < it.Lq;
         const bool valid_b = ra + 8 < tile_rows && tok_b < it.Lq;
         if ((lane & 3) == 0) {
-            if (valid_a)
+            if (valid_a && ATTN_IN_BOUNDS(it.q0 + tok_a < p.total_q, p.status))
                 p.lse[static_cast<size_t>(it.kvh * g + ra % g) * p.total_q + it.q0 + tok_a] =
                     l_a > 0.f ? (m_a + __log2f(l_a)) * kLn2 : -INFINITY;
-            if (valid_b)
+            if (valid_b && ATTN_IN_BOUNDS(it.q0 + tok_b < p.total_q, p.status))
                 p.lse[static_cast<size_t>(it.kvh * g + (ra + 8) % g) * p.total_q + it.q0 + tok_b] =
                     l_b > 0.f ? (m_b + __log2f(l_b)) * kLn2 : -INFINITY;
         }

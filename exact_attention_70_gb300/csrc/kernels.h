@@ -13,6 +13,20 @@ namespace attn {
 constexpr unsigned kStatusTimeout = 1u;
 constexpr unsigned kStatusBounds = 2u;
 
+// Opt-in device bounds checks, for debugging (build with -DATTN_CHECK_BOUNDS, which
+// exact_attention_70_gb300.build does for build(check_bounds=True)): a global store or a TMA
+// coordinate that would leave its tensor raises the bounds bit of the status word and is
+// skipped.  In the default build the check is the constant true and generates no code.
+#ifdef ATTN_CHECK_BOUNDS
+__device__ __forceinline__ bool in_bounds(bool ok, unsigned* status) {
+    if (!ok) atomicOr(status, kStatusBounds);
+    return ok;
+}
+#define ATTN_IN_BOUNDS(cond, status) ::attn::in_bounds((cond), (status))
+#else
+#define ATTN_IN_BOUNDS(cond, status) true
+#endif
+
 // ---- prefill ----------------------------------------------------------------------------
 
 constexpr int kFwdBlockN = 128;     // keys per KV tile

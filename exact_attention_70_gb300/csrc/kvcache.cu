@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(256) kvcache_append_kernel(const AppendParams 
             const size_t dst =
                 ((static_cast<size_t>(page) * p.page_size + pos % p.page_size) * p.Hkv + kvh) * p.d + e0;
             const size_t src = (static_cast<size_t>(t) * p.Hkv + kvh) * p.d;
+            if (!ATTN_IN_BOUNDS(t < p.total_q && kvh < p.Hkv && e0 + 8 <= p.d, p.status)) continue;
             if (r < p.Hkv) {
                 const uint4 w = p.rot_dim > 0 ? rotate8(p, p.k_new + src, e0, pos)
                                               : *reinterpret_cast<const uint4*>(p.k_new + src + e0);
@@ -131,6 +132,7 @@ __global__ void __launch_bounds__(256) kvcache_append_kernel(const AppendParams 
         } else {  // rotated query row of head r - 2 Hkv
             const int h = r - 2 * p.Hkv;
             const size_t row = (static_cast<size_t>(t) * p.Hq + h) * p.d;
+            if (!ATTN_IN_BOUNDS(t < p.total_q && h < p.Hq && e0 + 8 <= p.d, p.status)) continue;
             *reinterpret_cast<uint4*>(p.q_rot + row + e0) = rotate8(p, p.q + row, e0, pos);
         }
     }

@@ -268,3 +268,13 @@ def test_quantize_arguments_are_checked(lib):
     assert call(13, None) == -1             # null q8
     assert call(12, P(4098)) == -1          # misaligned signs
     assert call(14, P(4097)) == -1          # misaligned q_scale
+
+
+def test_bounds_checking_build_exports_every_declared_symbol():
+    """The debugging library (kernels compiled with -DATTN_CHECK_BOUNDS) builds and has the
+    same interface as the regular one."""
+    path = attn_build.build(check_bounds=True)
+    assert path != attn_build.LIB
+    checked = ctypes.CDLL(path)
+    for n in declared_functions():
+        assert ctypes.cast(getattr(checked, n), ctypes.c_void_p).value, n
