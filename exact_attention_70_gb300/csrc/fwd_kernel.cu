@@ -458,8 +458,13 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
 #pragma unroll
     for (int c = 0; c < 4; ++c)
         st_addr[c] = p_tile + st_row * 128 + ((((2 * c + st_dc) ^ lane) & 7) << 4);
-    // log2(e) times what turns an S value into a logit (with modifiers S is made a logit first)
-    const float sl2 = kMods ? kLog2e : p.scale_log2;
+    // log2(e) times what turns an S value into a logit (a softcap makes S a logit first)
+    const float sl2 = (kMods && p.softcap > 0.f) ? kLog2e : p.scale_log2;
+    // ALiBi biases are added to S in S's own units (the logit over the scale when S is not a
+    // logit yet), and for causal attention every visible key lies at or before the query's
+    // position, so the bias is linear in the key: slope (key - pos)
+    const float alibi_unit = (kMods && !(p.softcap > 0.f)) ? 1.f / p.scale : 1.f;
+    const bool alibi_linear = p.causal || p.wr == 0;
     const uint64_t sl2x2 = f2_make(sl2, sl2);
     const int G = gridDim.x, cta = blockIdx.x;
     const int g = p.g;
@@ -487,8 +492,8 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
         float slope_a = 0.f, slope_b = 0.f, pos_a = 0.f, pos_b = 0.f;
         if constexpr (kMods) {
             if (p.alibi != nullptr) {
-                slope_a = p.alibi[it.kvh * g + ra % g];
-                slope_b = p.alibi[it.kvh * g + (ra + 8) % g];
+                slope_a = p.alibi[it.kvh * g + ra % g] * alibi_unit;
+                slope_b = p.alibi[it.kvh * g + (ra + 8) % g] * alibi_unit;
                 pos_a = static_cast<float>(tv.tok0 + ra / g + it.Lk - it.Lq);
                 pos_b = static_cast<float>(tv.tok0 + (ra + 8) / g + it.Lk - it.Lq);
             }
@@ -515,32 +520,70 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(s_free);
+                // per-row constants of this block added to the logits in log2 units (ALiBi)
+                float ca = 0.f, cb = 0.f;    // this thread's columns
+                float qa = 0.f, qb = 0.f;    // S-unit shift of its columns to the block start
+                float ra0 = 0.f, rb0 = 0.f;  // the rows' constants at the block start
                 if constexpr (kMods) {
-                    // logits: scale, softcap c tanh(x / c) with tanh x = 1 - 2 / (e^(2x) + 1),
+                    // softcap c tanh(x / c) of the scaled score with tanh x = 1 - 2 / (e^(2x) + 1),
                     // then the ALiBi bias; the element mask below comes after them
+                    // (pairs of scores through the paired fp32 operations: the same IEEE
+                    // roundings as scalar ones, half the instructions)
                     if (p.softcap > 0.f) {
                         const float k2 = 2.f * kLog2e * p.scale / p.softcap;
+                        const uint64_t k2x2 = f2_make(k2, k2), one2 = f2_make(1.f, 1.f);
+                        const uint64_t mtwo2 = f2_make(-2.f, -2.f);
+                        const uint64_t cap2 = f2_make(p.softcap, p.softcap);
 #pragma unroll
-                        for (int c = 0; c < 64; ++c) {
-                            const float y = ex2_approx(__uint_as_float(s[c]) * k2);
-                            s[c] = __float_as_uint(p.softcap * (1.f - 2.f * rcp_approx(1.f + y)));
+                        for (int c = 0; c < 64; c += 2) {
+                            float y0, y1, r0, r1;
+                            f2_split(f2_mul(f2_make(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), k2x2),
+                                     y0, y1);
+                            f2_split(f2_add(f2_make(ex2_approx(y0), ex2_approx(y1)), one2), r0, r1);
+                            f2_split(f2_mul(f2_fma(f2_make(rcp_approx(r0), rcp_approx(r1)), mtwo2, one2),
+                                            cap2),
+                                     y0, y1);
+                            s[c] = __float_as_uint(y0);
+                            s[c + 1] = __float_as_uint(y1);
                         }
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            s[c] = __float_as_uint(__uint_as_float(s[c]) * p.scale);
                     }
-                    if (p.alibi != nullptr) {
+                    if (p.alibi != nullptr && alibi_linear) {
+                        // slope (key - pos) = slope (8 c + e) + slope (key0 - pos): one FFMA per
+                        // score with a constant, and a per-row constant of the block
                         const float key0 = static_cast<float>(j * kFwdBlockN + cpair);
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
 #pragma unroll
                             for (int e = 0; e < 2; ++e) {
-                                const float key = key0 + static_cast<float>(8 * c + e);
+                                const float o = static_cast<float>(8 * c + e);
+                                s[4 * c + e] = __float_as_uint(fmaf(slope_a, o, __uint_as_float(s[4 * c + e])));
+                                s[4 * c + 2 + e] =
+                                    __float_as_uint(fmaf(slope_b, o, __uint_as_float(s[4 * c + 2 + e])));
+                            }
+                        }
+                        ca = slope_a * (key0 - pos_a) * sl2;
+                        cb = slope_b * (key0 - pos_b) * sl2;
+                        // the four threads of a row hold columns key0 = block start + cpair:
+                        // their maxima below are moved to the block start so the quad agrees
+                        qa = slope_a * static_cast<float>(cpair);
+                        qb = slope_b * static_cast<float>(cpair);
+                        ra0 = slope_a * (static_cast<float>(j * kFwdBlockN) - pos_a) * sl2;
+                        rb0 = slope_b * (static_cast<float>(j * kFwdBlockN) - pos_b) * sl2;
+                    } else if (p.alibi != nullptr) {
+                        // -slope |pos - key| with key = key0 + 8 c + e: (pos - key0) once per
+                        // block, then one subtraction of a constant per score (all values are
+                        // integers below 2^24, exact in fp32)
+                        const float key0 = static_cast<float>(j * kFwdBlockN + cpair);
+                        const float da = pos_a - key0, db = pos_b - key0;
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const float o = static_cast<float>(8 * c + e);
                                 s[4 * c + e] = __float_as_uint(
-                                    fmaf(-slope_a, fabsf(pos_a - key), __uint_as_float(s[4 * c + e])));
+                                    fmaf(-slope_a, fabsf(da - o), __uint_as_float(s[4 * c + e])));
                                 s[4 * c + 2 + e] = __float_as_uint(
-                                    fmaf(-slope_b, fabsf(pos_b - key), __uint_as_float(s[4 * c + 2 + e])));
+                                    fmaf(-slope_b, fabsf(db - o), __uint_as_float(s[4 * c + 2 + e])));
                             }
                         }
                     }
@@ -577,11 +620,22 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
                     xb1 = fmax3(xb1, __uint_as_float(s[4 * c + 3]), __uint_as_float(s[4 * c + 7]));
                 }
                 float mxa = fmaxf(xa0, xa1), mxb = fmaxf(xb0, xb1);
+                if constexpr (kMods) {
+                    mxa += qa;
+                    mxb += qb;
+                }
                 mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 1));
                 mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 1));
                 mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 2));
                 mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
-                const float mba = mxa * sl2, mbb = mxb * sl2;
+                float mba, mbb;
+                if constexpr (kMods) {
+                    mba = fmaf(mxa, sl2, ra0);
+                    mbb = fmaf(mxb, sl2, rb0);
+                } else {
+                    mba = mxa * sl2;
+                    mbb = mxb * sl2;
+                }
                 const bool need_a = mba > m_a + kRescaleThreshold;
                 const bool need_b = mbb > m_b + kRescaleThreshold;
                 const float mna = need_a ? mba : m_a, mnb = need_b ? mbb : m_b;
@@ -593,7 +647,14 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
                 m_b = mnb;
                 const float ra_ref = (m_a == -INFINITY) ? 0.f : m_a;
                 const float rb_ref = (m_b == -INFINITY) ? 0.f : m_b;
-                const uint64_t nma = f2_make(-ra_ref, -ra_ref), nmb = f2_make(-rb_ref, -rb_ref);
+                uint64_t nma, nmb;
+                if constexpr (kMods) {
+                    nma = f2_make(ca - ra_ref, ca - ra_ref);
+                    nmb = f2_make(cb - rb_ref, cb - rb_ref);
+                } else {
+                    nma = f2_make(-ra_ref, -ra_ref);
+                    nmb = f2_make(-rb_ref, -rb_ref);
+                }
                 // P = exp2(s * scale*log2e - m): paired FFMA, MUFU ex2, paired sums
                 uint64_t suma = 0, sumb = 0;
                 uint32_t pka[16], pkb[16];
