@@ -59,6 +59,8 @@ def load():
             lib.attn_get_device_status.argtypes = [P]
             lib.attn_selftest_wait_timeout.restype = i32
             lib.attn_selftest_wait_timeout.argtypes = [P]
+            lib.attn_selftest_softcap.restype = i32
+            lib.attn_selftest_softcap.argtypes = [P, P, i32, f32, f32, P]
             lib.attn_fwd_kvcache.restype = i32
             lib.attn_fwd_kvcache.argtypes = [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, P, P,
                                              i32, i32, i32, i32, i32, i32, i32, i32, i32,
@@ -149,6 +151,18 @@ def attn_get_device_status(stream=None) -> int:
 def attn_selftest_wait_timeout(stream=None) -> int:
     """Launch the bounded-wait self-test kernel (its wait runs out after 20 ms)."""
     return int(load().attn_selftest_wait_timeout(_stream(stream)))
+
+
+def attn_selftest_softcap(scores, softmax_scale: float, softcap: float, stream=None):
+    """softcap * tanh(softmax_scale * scores / softcap) as the modifier kernel computes it
+    (scores: contiguous device fp32, even length)."""
+    _check(scores, "scores", torch.float32, 1)
+    out = torch.empty_like(scores)
+    rc = load().attn_selftest_softcap(_ptr(scores), _ptr(out), scores.numel(),
+                                      float(softmax_scale), float(softcap), _stream(stream))
+    if rc != 0:
+        raise AttnError(rc, "attn_selftest_softcap")
+    return out
 
 
 def _workspace(nbytes, device, workspace):

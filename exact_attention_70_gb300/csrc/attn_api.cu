@@ -104,9 +104,20 @@ long long fwd_capacity_pairs(int batch, int max_seqlen_q, int g) {
     return static_cast<long long>(batch) * ((max_seqlen_q + per - 1) / per);
 }
 
-bool scale_ok(float s) { return isfinite(s) && s > 0.f; }
+// a positive, finite, normal fp32 (its reciprocal is finite too)
+bool scale_ok(float s) { return isfinite(s) && s >= 1.17549435e-38f; }
 
 constexpr float kLog2eF = 1.44269504088896340736f;
+
+// KV heads per group of the forward work list: as many as keep the group's K and V (all
+// sequences) within 32 MiB, about a quarter of the L2, so the CTAs working on one group find
+// the blocks other CTAs of the group already fetched.
+int fwd_heads_per_group(int total_k, int nheads_kv, int head_dim) {
+    const long long per_head = 4ll * total_k * head_dim;  // K and V, bf16
+    if (per_head <= 0) return nheads_kv;
+    const long long n = (32ll << 20) / per_head;
+    return static_cast<int>(n < 1 ? 1 : (n > nheads_kv ? nheads_kv : n));
+}
 
 }  // namespace
 }  // namespace attn
@@ -166,7 +177,8 @@ attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* out, f
                        int causal, int window_left, int window_right, void* workspace,
                        size_t workspace_bytes, void* stream, float softcap,
                        const float* alibi_slopes) {
-    if (!(softcap >= 0.f) || softcap > 1e30f || (alibi_slopes && !aligned(alibi_slopes, 4)))
+    if (!(softcap == 0.f || (softcap >= 0x1p-20f && softcap <= 1e30f)) ||
+        (alibi_slopes && !aligned(alibi_slopes, 4)))
         return ATTN_ERR_INVALID_ARG;
     if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
         nheads_q <= 0 || nheads_kv <= 0 || window_left < -1 || window_right < -1 ||
@@ -223,6 +235,7 @@ attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* out, f
     pp.causal = causal ? 1 : 0;
     pp.wl = window_left;
     pp.wr = window_right;
+    pp.heads_per_group = fwd_heads_per_group(total_k, nheads_kv, head_dim);
 
     FwdParams fp;
     memset(&fp, 0, sizeof(fp));
@@ -522,6 +535,7 @@ attn_status_t attn_fwd_kvcache(const void* q, const void* k_new, const void* v_n
     pp.causal = causal ? 1 : 0;
     pp.wl = window_left;
     pp.wr = window_right;
+    pp.heads_per_group = nheads_kv;  // one group: the cache's layout is the caller's
 
     // 3. attention over the cache, K/V gathered through block_table
     const int box_rows = page_size < kFwdBlockN ? page_size : kFwdBlockN;
@@ -761,6 +775,21 @@ attn_status_t attn_selftest_wait_timeout(void* stream) {
     attn_status_t st = device_state(&dev);
     if (st != ATTN_OK) return st;
     if (launch_watchdog_selftest(dev->status, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+attn_status_t attn_selftest_softcap(const float* scores, float* out, int n, float softmax_scale,
+                                    float softcap, void* stream) {
+    if (n < 0 || (n & 1) || !scale_ok(softmax_scale) || !(softcap >= 0x1p-20f && softcap <= 1e30f))
+        return ATTN_ERR_INVALID_ARG;
+    if (n == 0) return ATTN_OK;
+    if (!scores || !out || !aligned(scores, 8) || !aligned(out, 8)) return ATTN_ERR_INVALID_ARG;
+    DeviceState* dev = nullptr;
+    attn_status_t st = device_state(&dev);
+    if (st != ATTN_OK) return st;
+    if (launch_softcap_selftest(scores, out, n, softmax_scale, softcap,
+                                static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;
 }

@@ -33,6 +33,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "softcap.cuh"
 #include "tile_math.h"
 
 namespace attn {
@@ -74,6 +75,8 @@ struct FwdBars {
     uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_free[2];
     uint64_t epi_full[2], epi_free[2];  // O staged in P_t for a TMA store / the store read it
     uint64_t drain[2];
+    uint64_t idx_full[4], idx_empty[4];  // the claimed item indices (fwd_claim_item)
+    int idx_ring[4];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -150,11 +153,53 @@ __device__ __forceinline__ uint32_t ring_pos_v(int i, int m) {
     return i == m - 1 ? 2u * m - 1u : 2u * i + 2u;
 }
 
-// Persistent schedule: round k hands CTA c the item k*G + c (even rounds) or
-// k*G + G-1-c (odd rounds); the list is sorted longest-first, so the snake order evens out
-// the per-CTA totals.
-__device__ __forceinline__ int item_index(int k, int c, int G) {
-    return k * G + ((k & 1) ? (G - 1 - c) : c);
+// Persistent schedule with dynamic claims.  The work list comes in groups of KV heads, each
+// sorted longest-first; a CTA's TMA producer claims the next index from a global counter while
+// the CTA still works on its current item (after that item's first loads), so CTAs take items
+// in list order as they free up: the longest-first order evens out the finishing times, and
+// the CTAs running at any moment share the few KV heads of one or two groups, whose K/V
+// blocks then stay in L2 between the items that read them.  The producer hands each index to
+// the CTA's other roles through a four-slot ring in shared memory; every role derives the item
+// from the index (load_item), and -1 ends the loop.
+constexpr uint32_t kIdxRing = 4;
+constexpr uint32_t kIdxReaders = 18;  // the two MMA issuers and the 16 softmax warps
+
+// The producer's claim of ring position r (false: a wait gave up).  Slot r % 4 last held
+// position r - 4, which every reader took before its own item r - 3.
+__device__ __forceinline__ bool fwd_claim_item(const FwdParams& p, FwdBars* bars,
+                                               const Watchdog& wd, int n_items, uint32_t r,
+                                               int& idx) {
+    const uint32_t slot = r % kIdxRing;
+    if (r >= kIdxRing && !wd.wait(&bars->idx_empty[slot], ((r / kIdxRing) - 1) & 1))
+        return false;
+    idx = atomicAdd(&p.header->next_item, 1);
+    if (idx >= n_items) idx = -1;
+    bars->idx_ring[slot] = idx;
+    mbar_arrive(&bars->idx_full[slot]);  // release: the index is visible to the readers
+    return true;
+}
+
+// The item index of ring position r for one reading thread, and r advanced (-2: a wait gave
+// up, -1: no more items).
+__device__ __forceinline__ int fwd_take_item(FwdBars* bars, const Watchdog& wd, uint32_t& r) {
+    const uint32_t slot = r % kIdxRing;
+    if (!wd.wait(&bars->idx_full[slot], (r / kIdxRing) & 1)) return -2;
+    const int idx = *reinterpret_cast<volatile int*>(&bars->idx_ring[slot]);
+    mbar_arrive(&bars->idx_empty[slot]);
+    ++r;
+    return idx;
+}
+
+// The same for a whole warp: lane 0 releases the slot once every lane has the index.
+__device__ __forceinline__ int fwd_take_item_warp(FwdBars* bars, const Watchdog& wd,
+                                                  uint32_t& r, int lane) {
+    const uint32_t slot = r % kIdxRing;
+    if (!__all_sync(0xffffffffu, wd.wait(&bars->idx_full[slot], (r / kIdxRing) & 1))) return -2;
+    const int idx = *reinterpret_cast<volatile int*>(&bars->idx_ring[slot]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->idx_empty[slot]);
+    ++r;
+    return idx;
 }
 
 // Wait, ignoring the abort flag, for a barrier phase that TMA or the tensor core still owes
@@ -182,13 +227,19 @@ __device__ void fwd_producer_loop(const FwdParams& p, uint8_t* smem, FwdBars* ba
     tma_prefetch_desc(&p.tm_q);
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
-    const int G = gridDim.x, c = blockIdx.x;
     const uint32_t q_box_bytes = 64u * p.g * p.tpt * 2u;
-    for (int k = 0; k * G < n_items; ++k) {
-        const int idx = item_index(k, c, G);
-        if (idx >= n_items) continue;
+    uint32_t claims = 0;
+    int idx;
+    if (!fwd_claim_item(p, bars, wd, n_items, claims++, idx)) return;
+    while (idx >= 0) {
         const Item it = load_item<kPaged>(p, idx);
-        if (!it.any) continue;
+        int next = -1;
+        bool claimed = false;
+        if (!it.any) {
+            if (!fwd_claim_item(p, bars, wd, n_items, claims++, next)) return;
+            idx = next;
+            continue;
+        }
         if (q_cnt > 0 && !wd.wait(&bars->q_empty, (q_cnt - 1) & 1)) return;
         uint32_t qbytes = 0;
 #pragma unroll
@@ -253,7 +304,15 @@ __device__ void fwd_producer_loop(const FwdParams& p, uint8_t* smem, FwdBars* ba
                                     it.kvh, row);
                 }
             }
+            // claim the next item two key blocks before this one's last load: late enough
+            // that claims follow the order in which CTAs free up, early enough that the
+            // claim's round trip is hidden behind the blocks still to come
+            if (!claimed && r == max(min(1, 2 * m - 1), 2 * m - 5)) {
+                if (!fwd_claim_item(p, bars, wd, n_items, claims++, next)) return;
+                claimed = true;
+            }
         }
+        idx = next;
     }
 }
 
@@ -288,13 +347,12 @@ __device__ void fwd_mma_s(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint
     const uint64_t dkv = sdesc_sw128(smem_u32(smem + C::kOffKV), 16, 1024);
     const uint32_t q_lo = static_cast<uint32_t>(dq), d_hi = static_cast<uint32_t>(dq >> 32);
     const uint32_t kv_lo = static_cast<uint32_t>(dkv);
-    const int G = gridDim.x, cta = blockIdx.x;
     uint32_t q_cnt = 0, kv_cnt = 0;
     uint32_t kpar = 0;                // per-slot parity of the K blocks consumed so far
     uint32_t s_cnt0 = 0, s_cnt1 = 0;  // S_t issued so far
-    for (int k = 0; k * G < n_items; ++k) {
-        const int idx = item_index(k, cta, G);
-        if (idx >= n_items) continue;
+    for (uint32_t rd = 0;;) {
+        const int idx = fwd_take_item(bars, wd, rd);
+        if (idx < 0) return;
         const Item it = load_item<kPaged>(p, idx);
         if (!it.any) continue;
         if (!wd.wait(&bars->q_full, q_cnt & 1)) return;
@@ -343,14 +401,13 @@ __device__ void fwd_mma_pv(const FwdParams& p, uint8_t* smem, FwdBars* bars, uin
     const uint64_t dv = sdesc_sw128(smem_u32(smem + C::kOffKV), C::kAtomBytes, 1024);
     const uint32_t p_lo = static_cast<uint32_t>(dp), p_hi = static_cast<uint32_t>(dp >> 32);
     const uint32_t v_lo = static_cast<uint32_t>(dv), v_hi = static_cast<uint32_t>(dv >> 32);
-    const int G = gridDim.x, cta = blockIdx.x;
     uint32_t kv_cnt = 0;
     uint32_t vpar = 0;                    // per-slot parity of the V blocks consumed so far
     uint32_t pv_cnt0 = 0, pv_cnt1 = 0;    // PV_t issued so far (== P_t consumed)
     uint32_t o_items0 = 0, o_items1 = 0;  // items in which tile t accumulated into O_t
-    for (int k = 0; k * G < n_items; ++k) {
-        const int idx = item_index(k, cta, G);
-        if (idx >= n_items) continue;
+    for (uint32_t rd = 0;;) {
+        const int idx = fwd_take_item(bars, wd, rd);
+        if (idx < 0) return;
         const Item it = load_item<kPaged>(p, idx);
         if (!it.any) continue;
         bool first0 = true, first1 = true;
@@ -458,23 +515,24 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
 #pragma unroll
     for (int c = 0; c < 4; ++c)
         st_addr[c] = p_tile + st_row * 128 + ((((2 * c + st_dc) ^ lane) & 7) << 4);
-    // log2(e) times what turns an S value into a logit (a softcap makes S a logit first)
-    const float sl2 = (kMods && p.softcap > 0.f) ? kLog2e : p.scale_log2;
-    // ALiBi biases are added to S in S's own units (the logit over the scale when S is not a
-    // logit yet), and for causal attention every visible key lies at or before the query's
-    // position, so the bias is linear in the key: slope (key - pos)
-    const float alibi_unit = (kMods && !(p.softcap > 0.f)) ? 1.f / p.scale : 1.f;
+    // log2(e) times what turns an S value into a logit: the scale, or c where a softcap has
+    // made S tanh(scale S / c)
+    const bool capped = kMods && p.softcap > 0.f;
+    const float sl2 = capped ? p.softcap * kLog2e : p.scale_log2;
+    // ALiBi biases are added to S in S's own units (the logit over the scale, or over c), and
+    // for causal attention every visible key lies at or before the query's position, so the
+    // bias is linear in the key: slope (key - pos)
+    const float alibi_unit = capped ? 1.f / p.softcap : 1.f / p.scale;
     const bool alibi_linear = p.causal || p.wr == 0;
     const uint64_t sl2x2 = f2_make(sl2, sl2);
-    const int G = gridDim.x, cta = blockIdx.x;
     const int g = p.g;
     const int tile_rows = g * p.tpt;
     uint32_t blk = 0;  // blocks of tile t processed so far (== S_t consumed == P_t produced)
     uint32_t kv_cnt = 0;  // K/V ring slots filled for earlier items (locates paged V blocks)
     uint32_t vpar = 0;    // per-slot parity of the V blocks loaded for earlier items (paged)
-    for (int kit = 0; kit * G < n_items; ++kit) {
-        const int idx = item_index(kit, cta, G);
-        if (idx >= n_items) continue;
+    for (uint32_t rd = 0;;) {
+        const int idx = fwd_take_item_warp(bars, wd, rd, lane);
+        if (idx < 0) break;
         const Item it = load_item<kPaged>(p, idx);
         const uint32_t kv_base = kv_cnt;
         const uint32_t vpar_item = vpar;
@@ -525,26 +583,17 @@ __device__ void fwd_softmax(const FwdParams& p, uint8_t* smem, FwdBars* bars, ui
                 float qa = 0.f, qb = 0.f;    // S-unit shift of its columns to the block start
                 float ra0 = 0.f, rb0 = 0.f;  // the rows' constants at the block start
                 if constexpr (kMods) {
-                    // softcap c tanh(x / c) of the scaled score with tanh x = 1 - 2 / (e^(2x) + 1),
-                    // then the ALiBi bias; the element mask below comes after them
-                    // (pairs of scores through the paired fp32 operations: the same IEEE
-                    // roundings as scalar ones, half the instructions)
-                    if (p.softcap > 0.f) {
-                        const float k2 = 2.f * kLog2e * p.scale / p.softcap;
-                        const uint64_t k2x2 = f2_make(k2, k2), one2 = f2_make(1.f, 1.f);
-                        const uint64_t mtwo2 = f2_make(-2.f, -2.f);
-                        const uint64_t cap2 = f2_make(p.softcap, p.softcap);
+                    // softcap: S -> tanh(scale S / c), c applied through sl2; then the ALiBi
+                    // bias; the element mask below comes after them
+                    if (capped) {
+                        const float ku = softcap_ku(p.scale, p.softcap);
+                        const uint64_t ku2 = f2_make(ku, ku);
 #pragma unroll
                         for (int c = 0; c < 64; c += 2) {
-                            float y0, y1, r0, r1;
-                            f2_split(f2_mul(f2_make(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), k2x2),
-                                     y0, y1);
-                            f2_split(f2_add(f2_make(ex2_approx(y0), ex2_approx(y1)), one2), r0, r1);
-                            f2_split(f2_mul(f2_fma(f2_make(rcp_approx(r0), rcp_approx(r1)), mtwo2, one2),
-                                            cap2),
-                                     y0, y1);
-                            s[c] = __float_as_uint(y0);
-                            s[c + 1] = __float_as_uint(y1);
+                            float s0 = __uint_as_float(s[c]), s1 = __uint_as_float(s[c + 1]);
+                            softcap_tanh2(s0, s1, ku2);
+                            s[c] = __float_as_uint(s0);
+                            s[c + 1] = __float_as_uint(s1);
                         }
                     }
                     if (p.alibi != nullptr && alibi_linear) {
@@ -901,6 +950,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             mbar_init(&bars->epi_free[t], 1);
             mbar_init(&bars->drain[t], 1);
         }
+        for (uint32_t i = 0; i < kIdxRing; ++i) {
+            mbar_init(&bars->idx_full[i], 1);
+            mbar_init(&bars->idx_empty[i], kIdxReaders);
+        }
         bars->abort_flag = 0;
         mbar_fence_init();
     }
@@ -1018,6 +1071,7 @@ __global__ void __launch_bounds__(kPrepThreads) fwd_prepare_kernel(FwdPrepParams
             atomicOr(p.status, kStatusBounds);
             p.header->n_items = 0;
             p.header->n_pairs = 0;
+            p.header->next_item = 0;
         }
         return;
     }
@@ -1040,6 +1094,7 @@ __global__ void __launch_bounds__(kPrepThreads) fwd_prepare_kernel(FwdPrepParams
             atomicOr(p.status, kStatusBounds);
             p.header->n_items = 0;
             p.header->n_pairs = 0;
+            p.header->next_item = 0;
         }
         return;
     }
@@ -1072,12 +1127,19 @@ __global__ void __launch_bounds__(kPrepThreads) fwd_prepare_kernel(FwdPrepParams
         const int b = lo, m = q - p.prefix[b];
         const int cost = item_cost(p, p.cu_q[b + 1] - p.cu_q[b], seq_keys(p, b), m);
         const int slot = atomicAdd(&hist[kPrepBins - 1 - min(cost, kPrepBins - 1)], 1);
-        for (int h = 0; h < p.Hkv; ++h)
-            p.items[static_cast<size_t>(slot) * p.Hkv + h] = make_int4(b, h, m, cost);
+        // groups of heads_per_group KV heads, one after the other; inside a group the pairs
+        // longest-first, each pair's heads side by side
+        for (int h = 0; h < p.Hkv; ++h) {
+            const int h0 = h - h % p.heads_per_group;
+            const int width = min(p.heads_per_group, p.Hkv - h0);
+            p.items[static_cast<size_t>(n_pairs) * h0 + static_cast<size_t>(slot) * width +
+                    (h - h0)] = make_int4(b, h, m, cost);
+        }
     }
     if (tid == 0) {
         p.header->n_pairs = n_pairs;
         p.header->n_items = n_pairs * p.Hkv;
+        p.header->next_item = 0;
     }
 }
 

@@ -39,7 +39,8 @@ constexpr int kPrepBins = 1024;     // cost histogram bins of the work-list sort
 struct FwdWorkspaceHeader {
     int n_items;
     int n_pairs;
-    int pad[62];
+    int next_item;  // the forward kernel's claim counter (reset by the work-list kernel)
+    int pad[61];
 };
 
 struct FwdPrepParams {
@@ -54,6 +55,7 @@ struct FwdPrepParams {
     int batch, total_q, total_k, max_seqlen_q, max_seqlen_k;
     int Hkv, tpt, capacity_pairs;
     int causal, wl, wr;
+    int heads_per_group;  // KV heads whose items are listed together (1..Hkv)
 };
 
 struct FwdParams {
@@ -66,7 +68,7 @@ struct FwdParams {
     const int* cu_q;
     const int* cu_k;            // contiguous K/V; null when paged
     const int4* items;
-    const FwdWorkspaceHeader* header;
+    FwdWorkspaceHeader* header;  // n_items, and the claim counter the kernel advances
     unsigned* status;
     int Hq, Hkv, g, tpt, total_q;
     int causal, wl, wr;
@@ -178,6 +180,8 @@ cudaError_t launch_quantize_fp8(const QuantParams& p, cudaStream_t stream);
 // ---- failure-path self-test ------------------------------------------------------------
 
 cudaError_t launch_watchdog_selftest(unsigned* status, cudaStream_t stream);
+cudaError_t launch_softcap_selftest(const float* s, float* out, int n, float scale, float softcap,
+                                    cudaStream_t stream);
 
 // ---- decode -------------------------------------------------------------------------------
 

@@ -68,7 +68,7 @@ typedef enum {
  *   max_seqlen_q, max_seqlen_k   upper bounds on the per-sequence lengths (sizing only)
  *   nheads_q, nheads_kv          nheads_q % nheads_kv == 0, group nheads_q/nheads_kv <= 128
  *   head_dim      64 or 128
- *   softmax_scale finite and > 0 (callers wanting the default pass head_dim^-0.5)
+ *   softmax_scale finite and >= FLT_MIN (callers wanting the default pass head_dim^-0.5)
  *   causal, window_left, window_right   see "Visibility"; window values >= -1
  *   workspace     device scratch of at least attn_fwd_workspace_bytes(...) bytes, holding the
  *                 tile work list; contents need not be initialised; not retained after the
@@ -107,7 +107,7 @@ size_t attn_fwd_workspace_bytes(int batch, int max_seqlen_q, int nheads_q, int n
  *   lse           device fp32 [batch, nheads_q], natural log
  *   batch, nheads_q, nheads_kv, head_dim, max_pages_per_seq, num_pages   host sizes;
  *                 head_dim 64 or 128; nheads_q % nheads_kv == 0
- *   softmax_scale finite and > 0
+ *   softmax_scale finite and >= FLT_MIN
  *   workspace     device scratch of attn_decode_workspace_bytes(batch, nheads_q, head_dim,
  *                 num_splits) bytes for the split partials (may be NULL when that is 0)
  *   stream        cudaStream_t
@@ -176,7 +176,7 @@ attn_status_t attn_decode_kvcache_noalloc(const void* q, const void* k_cache,
  *                (a, b) -> (a cos - b sin, a sin + b cos), computed in fp32, stored as bf16.
  *   out bf16 [total_q, nheads_q, head_dim]; lse fp32 [nheads_q, total_q] (natural log)
  *   head_dim 64 or 128; page_size a multiple of 16 that divides 128 or is a multiple of 128;
- *   rotary_dim a multiple of 16 (0 = none); softmax_scale > 0; windows -1 = unbounded.
+ *   rotary_dim a multiple of 16 (0 = none); softmax_scale finite and >= FLT_MIN; windows -1 = unbounded.
  *   workspace: attn_fwd_kvcache_workspace_bytes(...) bytes, 256-byte aligned.
  * Ownership: caller's buffers; nothing is allocated.  Errors: argument checks before any
  * launch; an out-of-range page id, position or rotary row raises ATTN_ERR_DEVICE_BOUNDS
@@ -232,7 +232,7 @@ size_t attn_bwd_workspace_bytes(int total_q, int nheads_q);
  *   alibi_slopes    device fp32 [nheads_q] or NULL: s -> s - slope_h * |i + Lk - Lq - j|
  *                   (query i at its bottom-right position, key j)
  * LSE is that of the modified scores.  Other arguments, layouts and errors as attn_fwd;
- * softcap must be finite and >= 0.
+ * softcap must be 0 or in [2^-20, 1e30].
  */
 attn_status_t attn_fwd_mods(const void* q, const void* k, const void* v, void* out, float* lse,
                             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch,
@@ -316,6 +316,17 @@ attn_status_t attn_get_device_status(void* stream);
  * the kernel is launched, ATTN_ERR_CUDA if the launch fails.
  */
 attn_status_t attn_selftest_wait_timeout(void* stream);
+
+/*
+ * Softcap check.  Writes out[i] = softcap * tanh(softmax_scale * scores[i] / softcap) for
+ * i < n, computed on `stream` by the device code attn_fwd_mods applies to each score
+ * (tanh u = 1 - 2 / (e^(2u) + 1) with the hardware exp2 and reciprocal, u = scale s / c).
+ * scores, out: device fp32 [n], 8-byte aligned, caller-owned; n even.
+ * Returns ATTN_ERR_INVALID_ARG for a bad n, pointer, scale or softcap (which must lie in
+ * [2^-20, 1e30]), ATTN_ERR_CUDA if the launch fails, else ATTN_OK.
+ */
+attn_status_t attn_selftest_softcap(const float* scores, float* out, int n, float softmax_scale,
+                                    float softcap, void* stream);
 
 /* Static description of a status code. */
 const char* attn_status_string(attn_status_t status);

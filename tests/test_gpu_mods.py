@@ -30,6 +30,9 @@ CASES = [
     ([200, 129], None, 4, 4, 64, False, (-1, -1), 2.0, True),
     ([400], [600], 4, 1, 128, True, (100, 0), 20.0, True),   # bottom-right, window
     ([260], None, 6, 2, 128, False, (40, 40), 0.0, True),    # g = 3
+    ([333], None, 4, 2, 128, True, (-1, -1), 64.0, False),   # largest cap of the polynomial form
+    ([333], None, 4, 2, 128, True, (-1, -1), 100.0, True),   # exp2 + reciprocal form
+    ([190, 70], None, 4, 4, 64, True, (-1, -1), 0.5, False),  # scores deep in saturation
 ]
 
 
@@ -83,3 +86,20 @@ def test_modifiers_repeatable_with_fresh_buffers(attn, idx):
         else:
             assert torch.equal(o, first[0]) and torch.equal(l, first[1]), f"rep {rep} differs"
         del filler
+
+
+@pytest.mark.parametrize("cap", [0.5, 2.0, 30.0, 64.0, 100.0, 1e4])
+def test_softcap_map_on_the_device(attn, cap):
+    """The kernel's softcap map, evaluated by the device code itself (attn_selftest_softcap),
+    against c tanh(scale s / c) in fp64: tanh u = 1 - 2 / (e^(2u) + 1) from the hardware exp2
+    and reciprocal stays within a few fp32 ulps of 1, times c, saturation included."""
+    scale = 128 ** -0.5
+    g = torch.Generator().manual_seed(int(cap * 10))
+    s = torch.cat([torch.linspace(-3000.0, 3000.0, 1 << 16),
+                   torch.randn(1 << 16, generator=g) * 4 * cap / scale,
+                   torch.tensor([0.0, -0.0, 1e-30, -1e-30, 1e-4, -1e-4, 3e30, -3e30])])
+    out = attn.attn_selftest_softcap(s.cuda(), scale, cap).cpu().double()
+    ref = cap * torch.tanh(scale * s.double() / cap)
+    err = (out - ref).abs().max().item()
+    assert err <= cap * 2e-6, (cap, err)
+    assert torch.all(out.abs() <= cap * (1 + 2 ** -21))

@@ -221,6 +221,14 @@ def test_modifier_arguments_are_checked(lib):
 
     assert call(19, -1.0) == -1              # negative softcap
     assert call(19, float("nan")) == -1
+    assert call(19, 1e-7) == -1              # below 2^-20
+    assert call(19, 2e30) == -1              # above 1e30
+    assert call(15, 1e-39) == -1             # subnormal scale (its reciprocal overflows)
+    sc = lib.attn_selftest_softcap
+    assert sc(fake, fake, 3, 0.1, 30.0, None) == -1   # odd n
+    assert sc(fake, fake, 2, 0.1, 1e-7, None) == -1   # softcap out of range
+    assert sc(fake, P(4100), 2, 0.1, 30.0, None) == -1  # misaligned out
+    assert sc(fake, fake, 0, 0.1, 30.0, None) == 0    # nothing to do
     assert call(20, P(4098)) == -1           # misaligned slopes
     assert call(7, 0) == 0                   # batch 0
 
