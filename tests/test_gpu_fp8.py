@@ -60,6 +60,9 @@ CASES = [
     dict(lq=[64, 200], lk=[500, 700], Hq=4, Hkv=2, causal=True),
     dict(lq=[300, 129], Hq=4, Hkv=2, causal=True, full_range=True),   # subnormals, +-448
     dict(lq=[200], lk=[450], Hq=2, Hkv=1, causal=False, full_range=True),
+    # 48 sequences of 0..289 tokens: more items than CTAs, so the persistent CTAs walk several
+    # (empty ones among them)
+    dict(lq=[(37 * i) % 290 for i in range(48)], Hq=4, Hkv=2, causal=True),
 ]
 
 

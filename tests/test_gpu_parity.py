@@ -74,6 +74,9 @@ PREFILL_SMALL = [
     ([300, 40], [100, 0], 4, 4, 128, True, (-1, -1)),              # Lk < Lq; a sequence with no keys
     ([260], [700], 4, 4, 128, False, (-1, -1)),
     ([1000], None, 8, 8, 128, True, (300, 0)),
+    # 48 sequences of 0..289 tokens: ~600 work items over the persistent CTAs, several claimed
+    # by each, empty sequences among them
+    ([(37 * i) % 290 for i in range(48)], None, 8, 2, 128, True, (-1, -1)),
 ]
 
 
