@@ -55,6 +55,9 @@ class L2Flush:
         import torch
         torch.sum(self.buf, dim=0, out=self.out)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Nominal GB300 figures, shown as a second denominator beside the measured ones: dense bf16
+# tensor-core peak and HBM3e bandwidth from the vendor's specification.
+NOMINAL_PEAKS = {"bf16_tflops": 2250.0, "hbm_gbs": 8000.0}
 PREFILL_CFG, DECODE_CFG = 2, 4
 
 
@@ -688,6 +691,8 @@ def main():
             "traffic": ncu_traffic("fwd_kernel", "fwd_kernel.cu"),
             "kernel": "fwd_kernel (prepare + persistent launch, CUDA events around attn_fwd)",
             "peak_source": f"{peak_src} bf16 dense burst",
+            "nominal_peak": NOMINAL_PEAKS["bf16_tflops"],
+            "nominal_frac": round(per_gpu_pre / NOMINAL_PEAKS["bf16_tflops"], 4),
         },
         "decode": {
             "value": round(dec_gbs, 2), "unit": "GB/s", "ms": round(r["dec_ms"], 5),
@@ -697,6 +702,8 @@ def main():
                 "traffic": ncu_traffic("decode_split_kernel", "decode_kernel.cu"),
                 "kernel": "decode_split_kernel + combine (CUDA events around attn_decode_kvcache)",
                 "peak_source": f"{peak_src} copy bandwidth",
+                "nominal_peak": NOMINAL_PEAKS["hbm_gbs"],
+                "nominal_frac": round(per_gpu_dec / NOMINAL_PEAKS["hbm_gbs"], 4),
             },
             "e2e": {"value": round(job_rate(r["d_bytes"], r["e2e_dec"], world) / 1e9, 2),
                     "unit": "GB/s", "h2d_bytes_per_step": r["h2d_dec"],
