@@ -319,6 +319,8 @@ attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
     const int g = nheads_q / nheads_kv;
     if (g > 128) return ATTN_ERR_UNSUPPORTED;
     if (batch == 0 || total_q == 0) return ATTN_OK;
+    // no keys anywhere: k8 may be an empty tensor without storage (its map is never read)
+    if (total_k == 0) k8 = v8t;
     if (!q8 || !k8 || !v8t || !q_scale || !k_scale || !v_scale || !out || !lse ||
         !cu_seqlens_q || !cu_seqlens_k || key_blocks == 0)
         return ATTN_ERR_INVALID_ARG;

@@ -247,7 +247,7 @@ attn_status_t attn_fwd_mods(const void* q, const void* k, const void* v, void* o
  * FlashAttention-3): Q, K and V as e4m3 bytes with block-wise fp32 scales, V re-laid out
  * key-major; the result is the attention of the dequantized values.
  *   q8      device u8 e4m3 [total_q, nheads_q, head_dim]
- *   k8      device u8 e4m3 [total_k, nheads_kv, head_dim]
+ *   k8      device u8 e4m3 [total_k, nheads_kv, head_dim] (may be NULL when total_k == 0)
  *   v8t     device u8 e4m3 [nheads_kv, head_dim, 128 * key_blocks]: V transposed; key t of
  *           sequence b sits in column 128 * kb0[b] + (t - cu_seqlens_k[b]), kb0 the prefix sum
  *           of ceil(Lk_b / 128); columns past a sequence's keys must hold finite values (zero)

@@ -77,6 +77,8 @@ PREFILL_SMALL = [
     # 48 sequences of 0..289 tokens: ~600 work items over the persistent CTAs, several claimed
     # by each, empty sequences among them
     ([(37 * i) % 290 for i in range(48)], None, 8, 2, 128, True, (-1, -1)),
+    # queries but no keys anywhere: every work item is claimed and has no key block
+    ([50, 70], [0, 0], 4, 2, 128, True, (-1, -1)),
 ]
 
 
