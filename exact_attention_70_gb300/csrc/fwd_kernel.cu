@@ -963,6 +963,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     const Watchdog wd{&bars->abort_flag, p.status};
+    // (launched as a programmatic dependent of the work-list kernel: the set-up above overlaps
+    // that kernel; the list is read only once it has finished)
+    griddep_wait();
     const int n_items = p.header->n_items;
 
     // Registers: launched at 96 per thread (640 threads); warpgroup 4 (TMA, two MMA issuers,
@@ -1051,6 +1054,7 @@ __global__ void __launch_bounds__(kPrepThreads) fwd_prepare_kernel(FwdPrepParams
     __shared__ int warp_tot[32];
     __shared__ int err;
     const int tid = threadIdx.x;
+    griddep_launch_dependents();  // the forward kernel may set up while the list is built
     if (tid == 0) err = 0;
     __syncthreads();
     // 1. the sequence boundaries must describe rows inside the tensors
@@ -1165,6 +1169,23 @@ cudaError_t launch_fwd_prepare(const FwdPrepParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// The forward kernel goes out as a programmatic dependent of the work-list kernel just before
+// it: its CTAs initialise barriers and TMEM while the list is built (griddep_wait in the kernel).
+template <int D, bool kPaged, bool kMods>
+cudaError_t launch_fwd_instance(const FwdParams& p, int grid, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kFwdThreads);
+    cfg.dynamicSmemBytes = FwdCfg<D>::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fwd_kernel<D, kPaged, kMods>, p);
+}
+
 // K/V through block_table when p.block_table is set, else contiguous; the score-modifier
 // instance when softcap or ALiBi is requested (contiguous K/V only).
 cudaError_t launch_fwd(const FwdParams& p, int head_dim, int grid, cudaStream_t stream) {
@@ -1172,21 +1193,13 @@ cudaError_t launch_fwd(const FwdParams& p, int head_dim, int grid, cudaStream_t 
     const bool mods = p.softcap > 0.f || p.alibi != nullptr;
     if (paged && mods) return cudaErrorInvalidValue;
     if (head_dim == 128) {
-        if (paged)
-            fwd_kernel<128, true, false><<<grid, kFwdThreads, FwdCfg<128>::kSmem, stream>>>(p);
-        else if (mods)
-            fwd_kernel<128, false, true><<<grid, kFwdThreads, FwdCfg<128>::kSmem, stream>>>(p);
-        else
-            fwd_kernel<128, false, false><<<grid, kFwdThreads, FwdCfg<128>::kSmem, stream>>>(p);
-    } else {
-        if (paged)
-            fwd_kernel<64, true, false><<<grid, kFwdThreads, FwdCfg<64>::kSmem, stream>>>(p);
-        else if (mods)
-            fwd_kernel<64, false, true><<<grid, kFwdThreads, FwdCfg<64>::kSmem, stream>>>(p);
-        else
-            fwd_kernel<64, false, false><<<grid, kFwdThreads, FwdCfg<64>::kSmem, stream>>>(p);
+        if (paged) return launch_fwd_instance<128, true, false>(p, grid, stream);
+        if (mods) return launch_fwd_instance<128, false, true>(p, grid, stream);
+        return launch_fwd_instance<128, false, false>(p, grid, stream);
     }
-    return cudaGetLastError();
+    if (paged) return launch_fwd_instance<64, true, false>(p, grid, stream);
+    if (mods) return launch_fwd_instance<64, false, true>(p, grid, stream);
+    return launch_fwd_instance<64, false, false>(p, grid, stream);
 }
 
 }  // namespace attn

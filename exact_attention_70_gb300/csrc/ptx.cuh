@@ -123,6 +123,19 @@ struct Watchdog {
     }
 };
 
+// ---- programmatic dependent launch ----------------------------------------------------------
+
+// Let the next kernel of the stream, if it was launched as a programmatic dependent, start
+// its CTAs now (its griddep_wait still waits for this grid to finish).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the grids this one depends on have finished and their writes are visible (a no-op
+// for a kernel launched without the programmatic-serialization attribute).
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---- register reallocation between warpgroups ----------------------------------------------
 
 template <uint32_t N>
