@@ -343,7 +343,8 @@ attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
     memset(&fp, 0, sizeof(fp));
     if (encode_3d_u8(&fp.tm_q, q8, head_dim, nheads_q, total_q, 128, g, tpt) != ATTN_OK ||
         encode_3d_u8(&fp.tm_k, k8, head_dim, nheads_kv, total_k > 0 ? total_k : 1, 128, 1, 128) != ATTN_OK ||
-        encode_3d_u8(&fp.tm_v, v8t, 128ull * key_blocks, head_dim, nheads_kv, 128, 128, 1) != ATTN_OK)
+        encode_3d_u8(&fp.tm_v, v8t, 128ull * key_blocks, head_dim, nheads_kv, 128, 128, 1) != ATTN_OK ||
+        encode_3d(&fp.tm_o, out, head_dim, nheads_q, total_q, g, tpt) != ATTN_OK)
         return ATTN_ERR_CUDA;
     fp.q_scale = q_scale;
     fp.k_scale = k_scale;

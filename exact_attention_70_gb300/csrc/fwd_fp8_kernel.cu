@@ -17,6 +17,9 @@
 //              normal grid covers P~ >= 2^-10);
 //   warp 8:    TMA of each item's two Q tiles and of its K and V^T blocks into three-stage
 //              rings, each block serving both tiles;
+//   (an item's O leaves by TMA tensor store from the tile's P buffers when the tile's rows all
+//   belong to its sequence, so the stores drain while the next item starts; ragged tiles store
+//   row by row)
 //   warp 9:    the MMA issuer: S_t(n) = Q_t K(n)^T (kind::f8f6f4, K = 32 per instruction) as
 //              soon as tile t's softmax holds S_t(n-1) in registers, then O_t += P_t(n-1) V(n-1)
 //              (A = P from shared memory, B = the V^T block, both K-major).
@@ -311,6 +314,17 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
         bool ok = true;
         int n = 0;  // key blocks of this CTA so far (barrier phases run on across items)
         uint32_t items = 0;
+        // A whole tile's O leaves through its two P buffers by TMA store; before P or O is
+        // written there again, the store must have read them (the same for all four warps of
+        // the tile, so the named barrier is met alike).
+        bool epi_pending = false;
+        auto release_staging = [&]() {
+            if (epi_pending) {
+                if (quarter == 0 && lane == 0) bulk_wait_group_read_all();
+                named_bar_sync(1 + t, 128);
+                epi_pending = false;
+            }
+        };
         for (int k = 0; k * G < n_items; ++k) {
             const int v = f8_item_index(k, cta, G);
             if (v >= n_items) continue;
@@ -415,6 +429,7 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
                 // buffer bn is free once P V of block n - 2 has read it
                 if (n >= 2)
                     ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->p_empty[t][bn], ((n - 2) >> 1) & 1));
+                release_staging();
                 // P = 2^4 exp2(x - m), x = s c; an empty row so far uses m = 0 (no -inf - -inf);
                 // each 16 keys go to shared memory as they are done
                 const float off = kPLog2 - (m_used == -INFINITY ? 0.f : m_used);
@@ -456,13 +471,21 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
             const int bh = p.batch * p.Hkv, grp = v % bh;
             const int eb = grp / p.Hkv, ekvh = grp % p.Hkv;
             const int eq0 = *reinterpret_cast<const volatile int*>(p.cu_q + eb);
+            const int eLq = *reinterpret_cast<const volatile int*>(p.cu_q + eb + 1) - eq0;
             const int etile = 2 * (pairs - 1 - v / bh) + t;
             const int etok = etile * p.tpt + r / p.g, ehead = ekvh * p.g + r % p.g;
             const float vs = p.v_scale[static_cast<size_t>(eb) * p.Hkv + ekvh];
             const float mul = l > 0.f ? vs / l : 0.f;
+            // A tile whose rows all belong to the sequence is staged in its two P buffers (free:
+            // every P V of the item has finished) in the layout of a 128-byte-swizzled TMA box
+            // {64 columns, g heads, tpt tokens} and stored by TMA, asynchronously; a ragged tile
+            // is stored row by row.
+            const bool whole = (etile + 1) * p.tpt <= eLq;
+            if (whole) release_staging();
             __nv_bfloat16* dst = p.out + (static_cast<size_t>(eq0 + etok) * p.Hq + ehead) * 128;
             const bool stored =
                 ATTN_IN_BOUNDS(!valid || (eq0 + etok < p.total_q && ehead < p.Hq), p.status);
+            const uint32_t stage = smem_u32(smem + kOffP + 2 * t * kAtom) + r * 128;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint32_t o[32];
@@ -473,26 +496,50 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = 0u;
                 }
-                if (valid && ok && stored) {
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * mul, __uint_as_float(o[2 * e + 1]) * mul);
+                if (whole) {
+                    // 16-byte chunk c (of 16) of the row: buffer c / 8, position (c % 8) ^ (r % 8)
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        const int c = 4 * q + v4;
+                        st_shared_v4(stage + static_cast<uint32_t>((c >> 3) * kAtom + (((c & 7) ^ (r & 7)) * 16)),
+                                     w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+                    }
+                } else if (valid && ok && stored) {
                     uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * q);
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4)
-                        d4[v4] = make_uint4(
-                            pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * mul, __uint_as_float(o[8 * v4 + 1]) * mul),
-                            pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * mul, __uint_as_float(o[8 * v4 + 3]) * mul),
-                            pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * mul, __uint_as_float(o[8 * v4 + 5]) * mul),
-                            pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * mul, __uint_as_float(o[8 * v4 + 7]) * mul));
+                        d4[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
                 }
             }
             // O_t has been read: the next item's first P V may overwrite it
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->o_free[t]);
+            if (whole) {
+                fence_proxy_async_smem();
+                named_bar_sync(1 + t, 128);
+                if (quarter == 0 && lane == 0) {
+                    const int row0 = eq0 + etile * p.tpt;
+                    if (ok && ATTN_IN_BOUNDS(row0 >= 0 && row0 + p.tpt <= p.total_q && (ekvh + 1) * p.g <= p.Hq,
+                                             p.status)) {
+                        tma_store_3d(&p.tm_o, smem + kOffP + 2 * t * kAtom, 0, ekvh * p.g, row0);
+                        tma_store_3d(&p.tm_o, smem + kOffP + (2 * t + 1) * kAtom, 64, ekvh * p.g, row0);
+                    }
+                    bulk_commit_group();
+                }
+                epi_pending = true;
+            }
             if (valid && ok && stored)
                 p.lse[static_cast<size_t>(ehead) * p.total_q + eq0 + etok] =
                     l > 0.f ? (m_used + log2f(l) - kPLog2) * 0.69314718055994531f : -INFINITY;
             ++items;
         }
+        // the O stores this thread issued have completed before the CTA's memory goes
+        if (quarter == 0 && lane == 0) bulk_wait_group_all();
     }
     __syncwarp();
     tc_fence_before();

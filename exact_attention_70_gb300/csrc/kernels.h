@@ -143,6 +143,7 @@ struct Fp8Params {
     CUtensorMap tm_q;   // 3-D over q8  [total_q, Hq, d] u8, box {d, g, tpt}
     CUtensorMap tm_k;   // 3-D over k8  [total_k, Hkv, d] u8, box {d, 1, 128}
     CUtensorMap tm_v;   // 3-D over v8t [Hkv, d, 128 nkb] u8, box {128, d, 1}
+    CUtensorMap tm_o;   // 3-D over out [total_q, Hq, d] bf16, box {64, g, tpt}: stores of whole tiles
     const float* q_scale;
     const float* k_scale;
     const float* v_scale;
