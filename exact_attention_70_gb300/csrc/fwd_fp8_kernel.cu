@@ -486,16 +486,20 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
             const bool stored =
                 ATTN_IN_BOUNDS(!valid || (eq0 + etok < p.total_q && ehead < p.Hq), p.status);
             const uint32_t stage = smem_u32(smem + kOffP + 2 * t * kAtom) + r * 128;
+            // the row's 128 columns in one go (one wait for the four loads)
+            uint32_t ob[128];
+            if (had_blocks && ok) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    tmem_ld32(tmem + lane_off + col_o + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(ob + 32 * q));
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int e = 0; e < 128; ++e) ob[e] = 0u;
+            }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                uint32_t o[32];
-                if (had_blocks && ok) {
-                    tmem_ld32(tmem + lane_off + col_o + 32 * q, o);
-                    tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = 0u;
-                }
+                const uint32_t* o = ob + 32 * q;
                 uint32_t w[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
