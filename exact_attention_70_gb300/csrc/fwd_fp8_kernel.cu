@@ -407,6 +407,11 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
                     l *= alpha;
                     m_used = xm;
                 }
+                // Buffer bn is free once P V of block n - 2 has read it.  Waited for before the
+                // rescale below: pv_done's phases are told apart by parity only, so the wait for
+                // P V n - 1 there is exact only once P V n - 2 is known to have finished.
+                if (n >= 2)
+                    ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->p_empty[t][bn], ((n - 2) >> 1) & 1));
                 if (__any_sync(0xffffffffu, grow && alpha != 1.f) && n > n0) {
                     // O_t holds earlier blocks of this item: wait for its last P V, then scale
                     // its rows
@@ -425,10 +430,10 @@ __global__ void __launch_bounds__(kF8Threads, 1) fwd_fp8_kernel(const __grid_con
                         }
                         tmem_wait_st();
                     }
+                    // the rescaled O_t before the P V that p_full releases (issued by another
+                    // thread): the stores are ordered before that arrive
+                    tc_fence_before();
                 }
-                // buffer bn is free once P V of block n - 2 has read it
-                if (n >= 2)
-                    ok = ok && __all_sync(0xffffffffu, wd.wait(&bars->p_empty[t][bn], ((n - 2) >> 1) & 1));
                 release_staging();
                 // P = 2^4 exp2(x - m), x = s c; an empty row so far uses m = 0 (no -inf - -inf);
                 // each 16 keys go to shared memory as they are done

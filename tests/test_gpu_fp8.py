@@ -66,6 +66,13 @@ CASES = [
     dict(lq=[(37 * i) % 290 for i in range(48)], Hq=4, Hkv=2, causal=True),
     # queries but no keys anywhere: items with no key block (O = 0, LSE = -inf)
     dict(lq=[50, 70], lk=[0, 0], Hq=4, Hkv=2, causal=False),
+    # long items (48 or more key blocks on average), where the O rescales of a tile meet
+    # P V products still in flight
+    dict(lq=[300, 129], lk=[6200, 6300], Hq=2, Hkv=1, causal=False, full_range=True),
+    dict(lq=[200, 64], lk=[12500, 12300], Hq=2, Hkv=1, causal=True),
+    dict(lq=[400], lk=[9000], Hq=2, Hkv=1, causal=False, window=(7000, 100)),
+    dict(lq=[(37 * i) % 290 for i in range(8)], lk=[6200 + 50 * i for i in range(8)], Hq=2,
+         Hkv=1, causal=False),
 ]
 
 
