@@ -601,6 +601,22 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
     const int g = nheads_q / nheads_kv;
     if (g > 128) return ATTN_ERR_UNSUPPORTED;
     if (batch == 0 || (total_q == 0 && total_k == 0)) return ATTN_OK;
+    if (total_q == 0 || total_k == 0) {
+        // One side without rows: with no queries every key's gradient is zero, with no keys
+        // every query's.  The empty side's tensors may have no storage (NULL).
+        void* g0 = total_q == 0 ? dk : dq;
+        void* g1 = total_q == 0 ? dv : nullptr;
+        const size_t bytes = static_cast<size_t>(total_q == 0 ? total_k : total_q) *
+                             static_cast<size_t>(total_q == 0 ? nheads_kv : nheads_q) *
+                             static_cast<size_t>(head_dim) * 2;
+        if (!g0 || !aligned(g0, 16) || (total_q == 0 && (!g1 || !aligned(g1, 16))))
+            return ATTN_ERR_INVALID_ARG;
+        const cudaStream_t s = static_cast<cudaStream_t>(stream);
+        if (cudaMemsetAsync(g0, 0, bytes, s) != cudaSuccess ||
+            (g1 && cudaMemsetAsync(g1, 0, bytes, s) != cudaSuccess))
+            return ATTN_ERR_CUDA;
+        return ATTN_OK;
+    }
     if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv || !cu_seqlens_q ||
         !cu_seqlens_k)
         return ATTN_ERR_INVALID_ARG;

@@ -210,7 +210,9 @@ size_t attn_fwd_kvcache_workspace_bytes(int batch, int total_q, int max_seqlen_q
  *   lse               fp32 [nheads_q, total_q] from attn_fwd (natural log)
  *   the remaining arguments as in attn_fwd (same sequences, mask, window and scale).
  *   workspace: attn_bwd_workspace_bytes(total_q, nheads_q) bytes, 256-byte aligned (D).
- * Rows without a visible key get zero gradient; keys no row sees get dk = dv = 0.
+ * Rows without a visible key get zero gradient; keys no row sees get dk = dv = 0.  With
+ * total_q == 0 only dk and dv are written (zeros) and q, out, dout, lse, dq may be NULL; with
+ * total_k == 0 only dq is (zeros) and k, v, dk, dv may be NULL.
  * Ownership: caller's buffers.  Errors: argument checks before any launch; inconsistent
  * cu_seqlens raise ATTN_ERR_DEVICE_BOUNDS.
  */

@@ -204,6 +204,14 @@ def test_bwd_arguments_are_rejected_before_any_launch(lib):
     assert call(4, P(4100)) == -1  # misaligned dout
     assert call(23, None) == -3    # workspace
     assert call(11, 0) == 0        # batch 0
+    # one side without rows: the other side's gradients must be given (and are zeroed on the
+    # device), the empty side's tensors may be NULL
+    a = list(args)
+    a[12], a[7] = 0, None          # total_q = 0 and no dk
+    assert f(*a) == -1
+    a = list(args)
+    a[13], a[6] = 0, P(4100)       # total_k = 0 and a misaligned dq
+    assert f(*a) == -1
     assert lib.attn_bwd_workspace_bytes(1000, 8) == (32000 + 255) // 256 * 256
     assert lib.attn_bwd_workspace_bytes(1001, 8) == (32032 + 255) // 256 * 256
 
