@@ -1,7 +1,7 @@
 """Seeded random configurations of every forward entry point against the fp64 oracle.
 
 Each seed draws a batch (1-5 sequences, empty and one-token ones among them), a head pairing
-(GQA ratios 1, 2, 3, 4, 8, 64), d in {64, 128}, causal or not, an optional window and lengths up to
+(GQA ratios 1, 2, 3, 4, 8, 64, 128), d in {64, 128}, causal or not, an optional window and lengths up to
 a few hundred tokens, then runs with those: the bf16 prefill, the FP8 forward (d = 128, small
 batches), the paged decode (page sizes 16-256, automatic and fixed split counts) and the
 chunked prefill over a paged cache (with or without rotary embedding).  Tolerances are those
@@ -22,7 +22,8 @@ from tests.parity import compare
 pytestmark = pytest.mark.gpu
 
 SEEDS = range(96)
-HEADS = [(1, 1), (2, 1), (4, 2), (6, 2), (8, 8), (16, 2), (12, 4), (32, 4), (64, 1), (128, 2)]
+HEADS = [(1, 1), (2, 1), (4, 2), (6, 2), (8, 8), (16, 2), (12, 4), (32, 4), (64, 1), (128, 2),
+         (128, 1)]
 
 
 @pytest.fixture(scope="module")
