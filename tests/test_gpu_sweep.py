@@ -23,7 +23,7 @@ pytestmark = pytest.mark.gpu
 
 SEEDS = range(96)
 HEADS = [(1, 1), (2, 1), (4, 2), (6, 2), (8, 8), (16, 2), (12, 4), (32, 4), (64, 1), (128, 2),
-         (128, 1)]
+         (128, 1), (8, 2)]
 
 
 @pytest.fixture(scope="module")
