@@ -14,8 +14,9 @@
 //       block kb0[b] + i (kb0 the prefix sum of ceil(Lk_b / 128)); unused blocks get scale 1;
 //   v8t [Hkv, d, 128 key_blocks]: V transposed, key t of sequence b in column
 //       128 kb0[b] + (t - k0), zero elsewhere; v_scale [batch, Hkv]: one per sequence and head.
-// Kernels: quant_rows_kernel (Q or K, one CTA per block and head, a warp per 16 rows, four
-// values per lane, the transform's butterflies across lanes by shuffles), quant_v_amax_kernel
+// Kernels: quant_rows_kernel (Q or K, one CTA per block and head, a warp per 16 rows, a row
+// per 8 lanes with 16 values a lane: four of the transform's seven butterfly stages inside the
+// lane, three across lanes by shuffles), quant_v_amax_kernel
 // (atomic max of |V| per sequence and head), quant_v_kernel (one CTA per key block and head,
 // transposed through shared memory), quant_v_finalize_kernel (amax -> scale).  All of it is
 // bandwidth-bound: each input byte is read once (V twice) and each output byte written once.
@@ -75,52 +76,69 @@ __global__ void __launch_bounds__(kQThreads) quant_rows_kernel(const __nv_bfloat
         t1 = min(min(cu_k[b + 1], t0 + 128), total);  // (rows are clamped to the tensor)
         if (t0 < 0) t0 = t1;
     }
-    float sg[4] = {1.f, 1.f, 1.f, 1.f};
-    if (signs != nullptr) {
+    // Each row is spread over a group of 8 lanes, 16 consecutive values a lane (element
+    // i = 16 j + k, j = lane % 8): the transform's stages h = 1 .. 8 stay inside the lane and
+    // h = 16, 32, 64 cross lanes j ^ 1, 2, 4.  A warp takes 4 rows at a time, 16 rows in all.
+    const int j = lane & 7, sub = lane >> 3;
+    float sg[16];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) sg[k] = signs[4 * lane + k];
+    for (int k = 0; k < 16; ++k) sg[k] = signs != nullptr ? signs[16 * j + k] : 1.f;
+    // all four rows' loads first, so that 128 bytes a lane are in flight at once
+    uint4 raw[4][2];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int t = t0 + 16 * warp + 4 * it + sub;
+        if (t < t1) {
+            const uint4* src4 = reinterpret_cast<const uint4*>(src + (static_cast<size_t>(t) * H + h) * 128 + 16 * j);
+            raw[it][0] = src4[0];
+            raw[it][1] = src4[1];
+        } else {
+            raw[it][0] = raw[it][1] = make_uint4(0u, 0u, 0u, 0u);
+        }
     }
-    // this warp's 16 rows, four consecutive values per lane
-    float x[16][4];
+    float x[4][16];
     float amax = 0.f;
 #pragma unroll
-    for (int rr = 0; rr < 16; ++rr) {
-        const int t = t0 + 16 * warp + rr;
-        if (t < t1) {
-            const uint2 u = *reinterpret_cast<const uint2*>(src + (static_cast<size_t>(t) * H + h) * 128 + 4 * lane);
-            x[rr][0] = __uint_as_float(u.x << 16);
-            x[rr][1] = __uint_as_float(u.x & 0xFFFF0000u);
-            x[rr][2] = __uint_as_float(u.y << 16);
-            x[rr][3] = __uint_as_float(u.y & 0xFFFF0000u);
-        } else {
+    for (int it = 0; it < 4; ++it) {
+        const int t = t0 + 16 * warp + 4 * it + sub;
+        float* v = x[it];
+        {
+            const uint32_t w[8] = {raw[it][0].x, raw[it][0].y, raw[it][0].z, raw[it][0].w,
+                                   raw[it][1].x, raw[it][1].y, raw[it][1].z, raw[it][1].w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) x[rr][k] = 0.f;
+            for (int q = 0; q < 8; ++q) {
+                v[2 * q] = __uint_as_float(w[q] << 16);
+                v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+            }
         }
         if (signs != nullptr) {
-            // element i = 4 lane + k; stages h = 1, 2 inside the lane, h = 4 .. 64 across lanes
 #pragma unroll
-            for (int k = 0; k < 4; ++k) x[rr][k] = __fmul_rn(x[rr][k], sg[k]);
-            float a, c;
-            a = x[rr][0]; c = x[rr][1]; x[rr][0] = __fadd_rn(a, c); x[rr][1] = __fsub_rn(a, c);
-            a = x[rr][2]; c = x[rr][3]; x[rr][2] = __fadd_rn(a, c); x[rr][3] = __fsub_rn(a, c);
-            a = x[rr][0]; c = x[rr][2]; x[rr][0] = __fadd_rn(a, c); x[rr][2] = __fsub_rn(a, c);
-            a = x[rr][1]; c = x[rr][3]; x[rr][1] = __fadd_rn(a, c); x[rr][3] = __fsub_rn(a, c);
+            for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(v[k], sg[k]);
+            // pair (lower, upper) -> (lower + upper, lower - upper), stage by stage
 #pragma unroll
-            for (int m = 1; m < 32; m <<= 1) {
-                const bool upper = (lane & m) != 0;
+            for (int hh = 1; hh < 16; hh <<= 1)
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float other = __shfl_xor_sync(0xffffffffu, x[rr][k], m);
-                    // pair (lower, upper) -> (lower + upper, lower - upper)
-                    x[rr][k] = upper ? __fsub_rn(other, x[rr][k]) : __fadd_rn(x[rr][k], other);
+                for (int k = 0; k < 16; ++k)
+                    if ((k & hh) == 0) {
+                        const float a = v[k], c = v[k + hh];
+                        v[k] = __fadd_rn(a, c);
+                        v[k + hh] = __fsub_rn(a, c);
+                    }
+#pragma unroll
+            for (int m = 1; m < 8; m <<= 1) {
+                const bool upper = (j & m) != 0;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float other = __shfl_xor_sync(0xffffffffu, v[k], m);
+                    v[k] = upper ? __fsub_rn(other, v[k]) : __fadd_rn(v[k], other);
                 }
             }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) x[rr][k] = __fmul_rn(x[rr][k], kInvSqrt128);
+            for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(v[k], kInvSqrt128);
         }
         if (t < t1) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fabsf(x[rr][k]));
+            for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(v[k]));
         }
     }
 #pragma unroll
@@ -135,12 +153,18 @@ __global__ void __launch_bounds__(kQThreads) quant_rows_kernel(const __nv_bfloat
     const float rcp = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
     if (threadIdx.x == 0) scale[static_cast<size_t>(h) * nblocks + blk] = s;
 #pragma unroll
-    for (int rr = 0; rr < 16; ++rr) {
-        const int t = t0 + 16 * warp + rr;
-        if (t < t1)
-            *reinterpret_cast<uint32_t*>(dst + (static_cast<size_t>(t) * H + h) * 128 + 4 * lane) =
-                e4m3x4(__fmul_rn(x[rr][0], rcp), __fmul_rn(x[rr][1], rcp),
-                       __fmul_rn(x[rr][2], rcp), __fmul_rn(x[rr][3], rcp));
+    for (int it = 0; it < 4; ++it) {
+        const int t = t0 + 16 * warp + 4 * it + sub;
+        const float* v = x[it];
+        if (t < t1) {
+            uint32_t c[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                c[q] = e4m3x4(__fmul_rn(v[4 * q], rcp), __fmul_rn(v[4 * q + 1], rcp),
+                              __fmul_rn(v[4 * q + 2], rcp), __fmul_rn(v[4 * q + 3], rcp));
+            *reinterpret_cast<uint4*>(dst + (static_cast<size_t>(t) * H + h) * 128 + 16 * j) =
+                make_uint4(c[0], c[1], c[2], c[3]);
+        }
     }
 }
 
@@ -152,13 +176,22 @@ __global__ void __launch_bounds__(256) quant_v_amax_kernel(const __nv_bfloat16* 
     const int b = blockIdx.y / Hkv, h = blockIdx.y % Hkv;
     const int k0 = max(cu_k[b], 0), k1 = min(cu_k[b + 1], total_k);
     const int t0 = k0 + 128 * blockIdx.x;
+    // 128 rows x 16 pieces of 8 values, eight pieces a thread, all loads issued before any use
+    uint4 u[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int idx = threadIdx.x + 256 * i;
+        const int t = t0 + idx / 16;
+        u[i] = t < k1 ? *reinterpret_cast<const uint4*>(v + (static_cast<size_t>(t) * Hkv + h) * 128 + 8 * (idx % 16))
+                      : make_uint4(0u, 0u, 0u, 0u);
+    }
     float m = 0.f;
-    for (int idx = threadIdx.x; idx < 128 * 32; idx += blockDim.x) {  // 128 rows x 32 lanes of 4
-        const int t = t0 + idx / 32;
-        if (t >= k1) break;
-        const uint2 u = *reinterpret_cast<const uint2*>(v + (static_cast<size_t>(t) * Hkv + h) * 128 + 4 * (idx % 32));
-        m = fmaxf(m, fmaxf(fmaxf(fabsf(__uint_as_float(u.x << 16)), fabsf(__uint_as_float(u.x & 0xFFFF0000u))),
-                           fmaxf(fabsf(__uint_as_float(u.y << 16)), fabsf(__uint_as_float(u.y & 0xFFFF0000u)))));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t w[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[q] << 16)), fabsf(__uint_as_float(w[q] & 0xFFFF0000u))));
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
